@@ -1,0 +1,205 @@
+/*
+ * pkv.h -- C ABI of the paged grouped-query decode-attention library (libpkv.so, CUDA, sm_103a).
+ *
+ * One decode step of attention over a block-table (paged) FP16 KV cache, as described in "PersistentKV:
+ * Page-Aware Decode Scheduling for Long-Context LLM Serving on Commodity GPUs" (arXiv 2606.26666):
+ *   - each query head hq of row b attends to its row's tokens through the row's block table; G = Hq / Hkv query
+ *     heads share KV head hkv = hq / G, and work is mapped by KV-head group so those G heads reuse every K/V tile
+ *     (abstract; gist.science technical summary, "Methodologie" 1, "Layout");
+ *   - sequence splitting: a row's pages are cut into disjoint ranges, each producing a partial online-softmax
+ *     state that a separate merge combines exactly ("Sequentie Splitting");
+ *   - row-local bounds: split ranges come from each row's true length; empty splits write a neutral state
+ *     ("Row-Local Bounds");
+ *   - the compact workqueue: a 1-D list of only the non-empty (row, KV head, split) tasks ("Compact Workqueue");
+ *   - a roofline-style host policy choosing the schedule and split size per step (abstract; "Calibrated
+ *     Adaptive Policy").
+ *
+ * Tensor layouts (all row-major, contiguous; fp16 = IEEE binary16):
+ *   q            [B][Hq][d]                           fp16, 16-byte aligned
+ *   k_pool       [num_pages][page_size][Hkv][d]       fp16, 16-byte aligned
+ *   v_pool       [num_pages][page_size][Hkv][d]       fp16, 16-byte aligned
+ *   block_table  [B][max_pages_per_seq]               int32; entry p of row b is the physical page of logical
+ *                                                     page p; entries past the row's last page are never read
+ *   seq_lens     [B]                                  int32, tokens per row this step (0 allowed)
+ *   out          [B][Hq][d]                           fp16, 16-byte aligned
+ * Token j of row b lives in slot j % page_size of page block_table[b][j / page_size].
+ * Supported: head_dim = 128, page_size = 16, G = Hq / Hkv in {1, 2, 4, 8, 16}, B <= PKV_MAX_BATCH.
+ *
+ * Ownership: the caller owns every buffer, including the workspace (sized by pkv_plan_t.ws_bytes, 256-byte
+ * aligned, prepared once with pkv_workspace_init). The library allocates no memory and keeps no per-call state;
+ * the only process-wide state is a once-per-device kernel attribute set-up.
+ * Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). Every device call only
+ * enqueues work and returns; pkv_plan is host-only and synchronous.
+ * Errors: every call returns PKV_OK (0) or a negative PKV_E_* code and enqueues nothing on error. Errors the
+ * kernels detect (a block-table entry outside the pool, a length beyond the table, a wait that timed out) are
+ * OR-ed into a status word in the workspace; read it with pkv_read_status. No call traps or aborts.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_VERSION 1
+
+#define PKV_OK 0
+#define PKV_E_INVAL (-1)        /* bad shape, negative size, inconsistent plan/problem */
+#define PKV_E_UNSUPPORTED (-2)  /* head_dim, page_size, group size or batch outside the supported set */
+#define PKV_E_NULLPTR (-3)      /* a required pointer is NULL */
+#define PKV_E_WS_TOO_SMALL (-4) /* workspace smaller than plan->ws_bytes */
+#define PKV_E_ALIGN (-5)        /* a pointer misses its required alignment */
+#define PKV_E_CUDA (-6)         /* a CUDA runtime call or kernel launch failed */
+
+/* bits of the device status word (pkv_read_status) */
+#define PKV_STATUS_BAD_PAGE 0x1u  /* a block-table entry read by the kernel is outside [0, num_pages) */
+#define PKV_STATUS_BAD_LEN 0x2u   /* a seq_len is negative or exceeds max_pages_per_seq * page_size */
+#define PKV_STATUS_TIMEOUT 0x4u   /* an internal pipeline wait exceeded its time limit; the kernel returned */
+#define PKV_STATUS_TASKS 0x8u     /* the device worklist outgrew the plan's task capacity (seq_lens changed
+                                     between pkv_plan and the launch; extra tasks were dropped), or a task or
+                                     row range in the workspace did not belong to the plan (it was skipped) */
+
+#define PKV_MAX_BATCH 4096
+
+/* schedules */
+#define PKV_VARIANT_SINGLE 0    /* one task per (row, KV head), output normalised in the decode kernel */
+#define PKV_VARIANT_SPLIT 1     /* rectangular grid over (row, KV head, split); empty splits write neutral states */
+#define PKV_VARIANT_WORKQUEUE 2 /* device-built compact list of non-empty tasks, pulled from an atomic queue */
+
+typedef struct pkv_problem {
+    int32_t batch;             /* B */
+    int32_t num_q_heads;       /* Hq */
+    int32_t num_kv_heads;      /* Hkv; Hq % Hkv == 0 */
+    int32_t head_dim;          /* d (128) */
+    int32_t page_size;         /* tokens per page (16) */
+    int32_t num_pages;         /* physical pages in each of k_pool / v_pool */
+    int32_t max_pages_per_seq; /* columns of block_table */
+} pkv_problem;
+
+/* Constants of the roofline cost model used by pkv_plan (microseconds and GB/s). */
+typedef struct pkv_policy {
+    double launch_us;      /* cost of one kernel launch in a step, including the gap to the previous kernel */
+    double hbm_gbs;        /* sustained KV streaming bandwidth of the decode kernel */
+    double cta_gbs;        /* streaming bandwidth one CTA reaches on its own (bounds a long task) */
+    double task_us;        /* fixed cost per task on one CTA (claim, q load, pipeline fill, state write) */
+    double merge_us;       /* fixed cost of the merge kernel beyond its launch */
+    double build_us;       /* fixed cost of the worklist builder beyond its launch */
+    double state_gbs;      /* bandwidth for writing + reading partial states */
+    int32_t ctas_per_sm;   /* resident decode CTAs per SM */
+    int32_t max_splits;    /* largest split count per row the policy may choose */
+    int32_t allow_variants;/* bit mask of PKV_VARIANT_* (1 << v) the policy may choose */
+    int32_t reserved;
+} pkv_policy;
+
+typedef struct pkv_plan_t {
+    int32_t variant;     /* PKV_VARIANT_* */
+    int32_t chunk_pages; /* c: pages per split; row b has S_b = ceil(ceil(L_b / page_size) / c) splits */
+    int32_t num_splits;  /* S = max_b S_b (extent of the rectangular grid) */
+    int32_t num_tasks;   /* tasks the decode kernel runs (single: B*Hkv; split: B*Hkv*S; wq: sum_b Hkv*S_b) */
+    int32_t grid_ctas;   /* persistent decode grid size */
+    int32_t group;       /* G = Hq / Hkv */
+    int32_t num_sms;     /* SM count the plan was made for */
+    int32_t reserved;
+    pkv_problem problem; /* copy of the problem the plan was made for; later calls must pass an equal one */
+    int64_t task_capacity;  /* task slots reserved in the workspace */
+    int64_t state_capacity; /* partial-state slots reserved in the workspace */
+    int64_t ws_bytes;       /* workspace bytes this plan needs */
+    int64_t off_row_off;    /* byte offsets inside the workspace: int32 row_off[B] */
+    int64_t off_row_splits; /*   int32 row_splits[B] */
+    int64_t off_tasks;      /*   int4 tasks[task_capacity] */
+    int64_t off_ml;         /*   float2 (m, l) per state */
+    int64_t off_acc;        /*   float acc[state_capacity][d] */
+    double predicted_us;    /* cost-model estimate for the step */
+    double kv_bytes;        /* algorithmic bytes of the step: K and V of every token + q + out */
+} pkv_plan_t;
+
+/* Packed task as the worklist builder stores it (16 bytes): x = row b, y = (h_kv << 16) | split s,
+ * z = first logical page, w = one past the last logical page. */
+typedef struct pkv_task {
+    int32_t row;
+    int32_t head_split;
+    int32_t page_begin;
+    int32_t page_end;
+} pkv_task;
+
+/* Workspace header at offset 0 (256 bytes). */
+typedef struct pkv_ws_header {
+    uint32_t queue_head;  /* next task to claim (workqueue) */
+    int32_t task_count;   /* tasks written by the last pkv_build_worklist */
+    uint32_t status;      /* PKV_STATUS_* bits, sticky until pkv_read_status clears them */
+    uint32_t reserved[61];
+} pkv_ws_header;
+
+/* Library version (PKV_VERSION). */
+int pkv_version(void);
+
+/* Text for a PKV_E_* code. */
+const char* pkv_strerror(int code);
+
+/* Validates a problem against the supported set. Host only. */
+int pkv_check_problem(const pkv_problem* problem);
+
+/* Fills *policy with the built-in cost-model constants (fitted on the calibration traces, seeds 0-4). */
+void pkv_policy_default(pkv_policy* policy);
+
+/*
+ * Plans one decode step (the "calibrated roofline-style policy" of the v2 abstract and of the gist.science
+ * summary, "Calibrated Adaptive Policy"): evaluates the cost model for the single-pass, split and workqueue
+ * schedules over a set of split sizes and keeps the cheapest. seq_lens_host [B] must equal the seq_lens the
+ * device calls will read. policy NULL = pkv_policy_default. num_sms = SMs of the target GPU. Host only.
+ */
+int pkv_plan(const pkv_problem* problem, const int32_t* seq_lens_host, int32_t num_sms, const pkv_policy* policy,
+             pkv_plan_t* plan);
+
+/* Same as pkv_plan with the schedule and split size fixed by the caller (chunk_pages >= 1; ignored for
+ * PKV_VARIANT_SINGLE). ctas_per_sm <= 0 means the default. Used by tests and calibration sweeps. */
+int pkv_plan_fixed(const pkv_problem* problem, const int32_t* seq_lens_host, int32_t num_sms, int32_t variant,
+                   int32_t chunk_pages, int32_t ctas_per_sm, pkv_plan_t* plan);
+
+/* Zeroes the workspace header (queue head, task count, status) on `stream`. Call once after allocating. */
+int pkv_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Worklist builder (compact workqueue, "Compact Workqueue"): from device seq_lens computes S_b, an exclusive
+ * prefix sum of Hkv*S_b, and writes the non-empty tasks in (b, h_kv, s) order, row_off/row_splits, the task count
+ * and resets the queue head. Only for plans with variant PKV_VARIANT_WORKQUEUE (returns PKV_E_INVAL otherwise).
+ */
+int pkv_build_worklist(const pkv_plan_t* plan, const pkv_problem* problem, const int32_t* seq_lens_dev, void* ws,
+                       size_t ws_bytes, void* stream);
+
+/*
+ * Decode kernel. single: writes out. split / workqueue: writes the partial (m, l, acc) state of every task's G
+ * query heads into the workspace (empty rectangular splits write m = -inf, l = 0, acc = 0); follow with
+ * pkv_merge. scale multiplies q.k (use 1/sqrt(head_dim)). out may be NULL unless the variant is single.
+ */
+int pkv_decode(const pkv_plan_t* plan, const pkv_problem* problem, const void* q, const void* k_pool,
+               const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev, float scale, void* ws,
+               size_t ws_bytes, void* out, void* stream);
+
+/*
+ * Log-sum-exp merge ("Sequentie Splitting": a separate merge combines the split states exactly):
+ * out[b,hq] = sum_s e^(m_s - M) acc_s / sum_s e^(m_s - M) l_s with M = max_s m_s over non-neutral states; a row
+ * with no non-empty state gets 0. For split and workqueue plans; a single plan returns PKV_OK without work.
+ */
+int pkv_merge(const pkv_plan_t* plan, const pkv_problem* problem, void* ws, size_t ws_bytes, void* out,
+              void* stream);
+
+/* Convenience: build (workqueue) + decode + merge for one step on one stream. */
+int pkv_decode_step(const pkv_plan_t* plan, const pkv_problem* problem, const void* q, const void* k_pool,
+                    const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev, float scale,
+                    void* ws, size_t ws_bytes, void* out, void* stream);
+
+/* Synchronises `stream`, copies the workspace status word to *status and clears it on the device. */
+int pkv_read_status(void* ws, size_t ws_bytes, void* stream, uint32_t* status);
+
+/* Number of kernel launches pkv_decode_step enqueues for this plan. */
+int pkv_plan_launches(const pkv_plan_t* plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,163 @@
+"""Python binding of libpkv.so: the C-ABI calls under the same names, taking torch tensors.
+
+Argument marshalling only: every step of the decode path (worklist build, decode, merge) runs in the library's
+CUDA kernels; the planner runs in the library's host code. PyTorch provides device memory and streams.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+
+import numpy as np
+import torch
+
+from ._lib import (PKV_VARIANT_SINGLE, PKV_VARIANT_SPLIT, PKV_VARIANT_WORKQUEUE, Plan, Policy, Problem, check,
+                   load)
+
+__all__ = [
+    "Problem", "Plan", "Policy", "pkv_version", "pkv_strerror", "pkv_check_problem", "pkv_policy_default",
+    "pkv_plan", "pkv_plan_fixed", "pkv_workspace_init", "pkv_build_worklist", "pkv_decode", "pkv_merge",
+    "pkv_decode_step", "pkv_read_status", "pkv_plan_launches", "make_problem", "alloc_workspace", "decode",
+    "PKV_VARIANT_SINGLE", "PKV_VARIANT_SPLIT", "PKV_VARIANT_WORKQUEUE",
+]
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name: str = "tensor") -> ctypes.c_void_p:
+    if t is None:
+        return ctypes.c_void_p(0)
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host_lens(seq_lens) -> np.ndarray:
+    if isinstance(seq_lens, torch.Tensor):
+        seq_lens = seq_lens.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+
+
+def pkv_version() -> int:
+    return load().pkv_version()
+
+
+def pkv_strerror(code: int) -> str:
+    return load().pkv_strerror(code).decode()
+
+
+def make_problem(batch, num_q_heads, num_kv_heads, head_dim, page_size, num_pages, max_pages_per_seq) -> Problem:
+    return Problem(int(batch), int(num_q_heads), int(num_kv_heads), int(head_dim), int(page_size), int(num_pages),
+                   int(max_pages_per_seq))
+
+
+def pkv_check_problem(problem: Problem) -> int:
+    return load().pkv_check_problem(ctypes.byref(problem))
+
+
+def pkv_policy_default() -> Policy:
+    pol = Policy()
+    load().pkv_policy_default(ctypes.byref(pol))
+    return pol
+
+
+def pkv_plan(problem: Problem, seq_lens_host, num_sms: int, policy: Policy | None = None) -> Plan:
+    lens = _host_lens(seq_lens_host)
+    plan = Plan()
+    pol = ctypes.byref(policy) if policy is not None else None
+    check(load().pkv_plan(ctypes.byref(problem), lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), int(num_sms),
+                          pol, ctypes.byref(plan)), "pkv_plan")
+    return plan
+
+
+def pkv_plan_fixed(problem: Problem, seq_lens_host, num_sms: int, variant: int, chunk_pages: int = 1,
+                   ctas_per_sm: int = 0) -> Plan:
+    lens = _host_lens(seq_lens_host)
+    plan = Plan()
+    check(load().pkv_plan_fixed(ctypes.byref(problem), lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                int(num_sms), int(variant), int(chunk_pages), int(ctas_per_sm), ctypes.byref(plan)),
+          "pkv_plan_fixed")
+    return plan
+
+
+def pkv_plan_launches(plan: Plan) -> int:
+    return load().pkv_plan_launches(ctypes.byref(plan))
+
+
+def alloc_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A uint8 CUDA tensor usable as workspace (torch's allocator returns 256-byte aligned blocks)."""
+    ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+    pkv_workspace_init(ws)
+    return ws
+
+
+def pkv_workspace_init(ws: torch.Tensor, stream=None) -> None:
+    check(load().pkv_workspace_init(_ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "pkv_workspace_init")
+
+
+def pkv_build_worklist(plan: Plan, problem: Problem, seq_lens: torch.Tensor, ws: torch.Tensor, stream=None) -> None:
+    check(load().pkv_build_worklist(ctypes.byref(plan), ctypes.byref(problem), _ptr(seq_lens, torch.int32, "seq_lens"),
+                                    _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "pkv_build_worklist")
+
+
+def _decode_args(plan, problem, q, k_pool, v_pool, block_table, seq_lens, scale, ws, out, stream):
+    return (ctypes.byref(plan), ctypes.byref(problem), _ptr(q, torch.float16, "q"), _ptr(k_pool, torch.float16, "k_pool"),
+            _ptr(v_pool, torch.float16, "v_pool"), _ptr(block_table, torch.int32, "block_table"),
+            _ptr(seq_lens, torch.int32, "seq_lens"), ctypes.c_float(scale), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+            _ptr(out, torch.float16, "out"), _stream(stream))
+
+
+def pkv_decode(plan, problem, q, k_pool, v_pool, block_table, seq_lens, scale, ws, out=None, stream=None) -> None:
+    check(load().pkv_decode(*_decode_args(plan, problem, q, k_pool, v_pool, block_table, seq_lens, scale, ws, out,
+                                          stream)), "pkv_decode")
+
+
+def pkv_merge(plan: Plan, problem: Problem, ws: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    check(load().pkv_merge(ctypes.byref(plan), ctypes.byref(problem), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+                           _ptr(out, torch.float16, "out"), _stream(stream)), "pkv_merge")
+
+
+def pkv_decode_step(plan, problem, q, k_pool, v_pool, block_table, seq_lens, scale, ws, out, stream=None) -> None:
+    check(load().pkv_decode_step(*_decode_args(plan, problem, q, k_pool, v_pool, block_table, seq_lens, scale, ws,
+                                               out, stream)), "pkv_decode_step")
+
+
+def pkv_read_status(ws: torch.Tensor, stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    check(load().pkv_read_status(_ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream), ctypes.byref(v)),
+          "pkv_read_status")
+    return int(v.value)
+
+
+def decode(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.Tensor,
+           seq_lens: torch.Tensor, seq_lens_host=None, out: torch.Tensor | None = None, plan: Plan | None = None,
+           ws: torch.Tensor | None = None, scale: float | None = None, stream=None) -> torch.Tensor:
+    """One decode step: plan (host), then build + decode + merge on the device. Returns out [B, Hq, d] fp16.
+
+    q [B,Hq,d] fp16; k_pool / v_pool [num_pages, page_size, Hkv, d] fp16; block_table [B, max_pages] int32;
+    seq_lens [B] int32 on the device; seq_lens_host, if given, must equal seq_lens (saves a device read).
+    """
+    B, Hq, d = q.shape
+    num_pages, ps, Hkv, d2 = k_pool.shape
+    problem = make_problem(B, Hq, Hkv, d, ps, num_pages, block_table.shape[1])
+    if plan is None:
+        host = seq_lens_host if seq_lens_host is not None else seq_lens
+        plan = pkv_plan(problem, host, torch.cuda.get_device_properties(q.device).multi_processor_count)
+    if ws is None or ws.numel() < plan.ws_bytes:
+        ws = alloc_workspace(plan.ws_bytes, q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    pkv_decode_step(plan, problem, q, k_pool, v_pool, block_table, seq_lens,
+                    1.0 / math.sqrt(d) if scale is None else float(scale), ws, out, stream)
+    return out

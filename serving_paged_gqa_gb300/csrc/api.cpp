@@ -1,0 +1,169 @@
+// C-ABI entry points of libpkv.so: argument validation and kernel launches (see include/pkv.h).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "pkv_internal.h"
+
+namespace {
+
+using namespace pkv;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool same_problem(const pkv_problem& a, const pkv_problem& b) { return std::memcmp(&a, &b, sizeof(a)) == 0; }
+
+int check_plan(const pkv_plan_t* plan, const pkv_problem* pr, const void* ws, size_t ws_bytes) {
+    if (!plan || !pr || !ws) return PKV_E_NULLPTR;
+    int rc = pkv_check_problem(pr);
+    if (rc != PKV_OK) return rc;
+    if (!same_problem(plan->problem, *pr)) return PKV_E_INVAL;
+    if (plan->variant < PKV_VARIANT_SINGLE || plan->variant > PKV_VARIANT_WORKQUEUE) return PKV_E_INVAL;
+    if (plan->group != pr->num_q_heads / pr->num_kv_heads || plan->grid_ctas <= 0 || plan->chunk_pages <= 0 ||
+        plan->num_splits <= 0 || plan->num_tasks < 0)
+        return PKV_E_INVAL;
+    if (!aligned(ws, kWsAlign)) return PKV_E_ALIGN;
+    if ((int64_t)ws_bytes < plan->ws_bytes) return PKV_E_WS_TOO_SMALL;
+    return PKV_OK;
+}
+
+template <typename T>
+T* at(void* ws, int64_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+int cuda_rc(int e) { return e == cudaSuccess ? PKV_OK : PKV_E_CUDA; }
+
+}  // namespace
+
+extern "C" int pkv_version(void) { return PKV_VERSION; }
+
+extern "C" const char* pkv_strerror(int code) {
+    switch (code) {
+        case PKV_OK: return "ok";
+        case PKV_E_INVAL: return "invalid argument";
+        case PKV_E_UNSUPPORTED: return "unsupported problem (head_dim 128, page_size 16, G in {1,2,4,8,16})";
+        case PKV_E_NULLPTR: return "null pointer";
+        case PKV_E_WS_TOO_SMALL: return "workspace smaller than plan->ws_bytes";
+        case PKV_E_ALIGN: return "misaligned pointer";
+        case PKV_E_CUDA: return "CUDA error";
+        default: return "unknown error";
+    }
+}
+
+extern "C" int pkv_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+    if (!ws) return PKV_E_NULLPTR;
+    if (ws_bytes < sizeof(pkv_ws_header)) return PKV_E_WS_TOO_SMALL;
+    if (!aligned(ws, kWsAlign)) return PKV_E_ALIGN;
+    return cuda_rc(cudaMemsetAsync(ws, 0, sizeof(pkv_ws_header), static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int pkv_build_worklist(const pkv_plan_t* plan, const pkv_problem* pr, const int32_t* seq_lens_dev,
+                                  void* ws, size_t ws_bytes, void* stream) {
+    int rc = check_plan(plan, pr, ws, ws_bytes);
+    if (rc != PKV_OK) return rc;
+    if (plan->variant != PKV_VARIANT_WORKQUEUE) return PKV_E_INVAL;
+    if (pr->batch > 0 && !seq_lens_dev) return PKV_E_NULLPTR;
+    if (!aligned(seq_lens_dev, 4)) return PKV_E_ALIGN;
+    BuildParams p{};
+    p.seq_lens = seq_lens_dev;
+    p.row_off = at<int32_t>(ws, plan->off_row_off);
+    p.row_splits = at<int32_t>(ws, plan->off_row_splits);
+    p.tasks = at<pkv_task>(ws, plan->off_tasks);
+    p.hdr = static_cast<pkv_ws_header*>(ws);
+    p.B = pr->batch;
+    p.Hkv = pr->num_kv_heads;
+    p.max_pages = pr->max_pages_per_seq;
+    p.chunk_pages = plan->chunk_pages;
+    p.task_capacity = (int32_t)plan->task_capacity;
+    const int64_t blocks = (plan->task_capacity + 1023) / 1024;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(blocks, 2 * (int64_t)plan->num_sms));
+    return cuda_rc(launch_build(p, grid, stream));
+}
+
+extern "C" int pkv_decode(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_pool,
+                          const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev, float scale,
+                          void* ws, size_t ws_bytes, void* out, void* stream) {
+    int rc = check_plan(plan, pr, ws, ws_bytes);
+    if (rc != PKV_OK) return rc;
+    if (pr->batch > 0 && (!q || !k_pool || !v_pool || !block_table || !seq_lens_dev)) return PKV_E_NULLPTR;
+    if (plan->variant == PKV_VARIANT_SINGLE && pr->batch > 0 && !out) return PKV_E_NULLPTR;
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+        !aligned(block_table, 4) || !aligned(seq_lens_dev, 4))
+        return PKV_E_ALIGN;
+    if (!(scale == scale)) return PKV_E_INVAL;
+    if (plan->num_tasks == 0) return PKV_OK;
+    DecodeParams p{};
+    p.q = q;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens_dev;
+    p.out = out;
+    p.ml = at<float>(ws, plan->off_ml);
+    p.acc = at<float>(ws, plan->off_acc);
+    p.tasks = at<const pkv_task>(ws, plan->off_tasks);
+    p.hdr = static_cast<pkv_ws_header*>(ws);
+    p.B = pr->batch;
+    p.Hq = pr->num_q_heads;
+    p.Hkv = pr->num_kv_heads;
+    p.num_pages = pr->num_pages;
+    p.max_pages = pr->max_pages_per_seq;
+    p.chunk_pages = plan->chunk_pages;
+    p.num_splits = plan->num_splits;
+    p.variant = plan->variant;
+    p.num_tasks = plan->num_tasks;
+    p.task_capacity = (int32_t)plan->task_capacity;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    return cuda_rc(launch_decode(p, plan->group, plan->grid_ctas, stream));
+}
+
+extern "C" int pkv_merge(const pkv_plan_t* plan, const pkv_problem* pr, void* ws, size_t ws_bytes, void* out,
+                         void* stream) {
+    int rc = check_plan(plan, pr, ws, ws_bytes);
+    if (rc != PKV_OK) return rc;
+    if (plan->variant == PKV_VARIANT_SINGLE) return PKV_OK;
+    if (pr->batch > 0 && !out) return PKV_E_NULLPTR;
+    if (!aligned(out, 16)) return PKV_E_ALIGN;
+    MergeParams p{};
+    p.ml = at<float>(ws, plan->off_ml);
+    p.acc = at<float>(ws, plan->off_acc);
+    p.row_off = at<int32_t>(ws, plan->off_row_off);
+    p.row_splits = at<int32_t>(ws, plan->off_row_splits);
+    p.out = out;
+    p.B = pr->batch;
+    p.Hq = pr->num_q_heads;
+    p.Hkv = pr->num_kv_heads;
+    p.num_splits = plan->num_splits;
+    p.variant = plan->variant;
+    p.status = &static_cast<pkv_ws_header*>(ws)->status;
+    p.task_capacity = plan->num_tasks;
+    return cuda_rc(launch_merge(p, stream));
+}
+
+extern "C" int pkv_decode_step(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_pool,
+                               const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev,
+                               float scale, void* ws, size_t ws_bytes, void* out, void* stream) {
+    int rc;
+    if (plan && plan->variant == PKV_VARIANT_WORKQUEUE) {
+        rc = pkv_build_worklist(plan, pr, seq_lens_dev, ws, ws_bytes, stream);
+        if (rc != PKV_OK) return rc;
+    }
+    rc = pkv_decode(plan, pr, q, k_pool, v_pool, block_table, seq_lens_dev, scale, ws, ws_bytes, out, stream);
+    if (rc != PKV_OK) return rc;
+    return pkv_merge(plan, pr, ws, ws_bytes, out, stream);
+}
+
+extern "C" int pkv_read_status(void* ws, size_t ws_bytes, void* stream, uint32_t* status) {
+    if (!ws || !status) return PKV_E_NULLPTR;
+    if (ws_bytes < sizeof(pkv_ws_header)) return PKV_E_WS_TOO_SMALL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    pkv_ws_header* hdr = static_cast<pkv_ws_header*>(ws);
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, &hdr->status, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return PKV_E_CUDA;
+    if (cudaMemsetAsync(&hdr->status, 0, sizeof(uint32_t), s) != cudaSuccess) return PKV_E_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_E_CUDA;
+    *status = v;
+    return PKV_OK;
+}

@@ -1,0 +1,502 @@
+// Persistent split-KV paged GQA decode kernel for sm_103a.
+//
+// Computes, for every task (row b, KV head h, page range [page_begin, page_end)), the online-softmax state of the
+// G = Hq/Hkv query heads that share KV head h ("PersistentKV: Page-Aware Decode Scheduling for Long-Context LLM
+// Serving on Commodity GPUs", abstract: work mapped by KV-head group so the grouped query heads reuse each K/V
+// tile; gist.science technical summary, "Methodologie" 1: native block-table execution, sequence splitting into
+// partial online-softmax states, row-local bounds with neutral states for empty splits, compact workqueue).
+//
+// CTA layout (one or two CTAs per SM, persistent over tasks):
+//   warp NCW+1  scheduler: claims tasks (atomic queue head for the workqueue, a static stride otherwise), reads the
+//               row length, publishes the task in a shared-memory slot and bulk-copies the G query rows into it;
+//   warp NCW    loader: walks the task's block-table entries (32 per load, prefetched one chunk ahead) and, per
+//               page, has 32 lanes issue one 256-byte bulk copy each (16 K rows + 16 V rows of KV head h) into a
+//               ring stage, completion counted in bytes on the stage's mbarrier;
+//   warps 0..NCW-1 consumers: page i of a task goes to warp i % NCW. Per page: S = Q K^T on mma.sync m16n8k16
+//               (rows = the G query heads, columns = the 16 tokens), masking of slots past the row length, online
+//               softmax in base 2 in registers with quad shuffles, O += P V on mma.sync. At the end of the task the
+//               NCW warps combine their states through shared memory and write either the normalised fp16 output
+//               (single-pass) or the partial state (m, l, acc) of each query head.
+// Every wait is bounded (global timer); on timeout the kernel sets PKV_STATUS_TIMEOUT in the workspace, the other
+// warps see an abort flag, the loader waits for its own copies in flight, and the CTA returns.
+#include <cuda_fp16.h>
+
+#include "pkv_internal.h"
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kSmemRow = kRowBytes + 16;           // padded row: ldmatrix over 8 rows hits 8 distinct bank groups
+constexpr int kStageBytes = 2 * kPageSize * kSmemRow;
+constexpr int kCombRow = kHeadDim + 8;             // floats per combined row (padding against bank conflicts)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct TaskSlot {
+    int32_t b, h, s, task, page_begin, npages, seq_len, pad;
+};
+
+template <int G, int NCW, int NS, int NTS>
+struct Layout {
+    static constexpr int kQRowsBytes = ((G * kSmemRow + 127) / 128) * 128;
+    static constexpr int off_stage = 0;
+    static constexpr int off_q = off_stage + NS * kStageBytes;
+    static constexpr int off_comb = off_q + NTS * kQRowsBytes;
+    static constexpr int comb_o_floats = NCW * G * kCombRow;
+    static constexpr int off_comb_ml = off_comb + comb_o_floats * 4;
+    static constexpr int off_slots = off_comb_ml + NCW * G * 8;
+    static constexpr int off_bars = ((off_slots + NTS * (int)sizeof(TaskSlot) + 15) / 16) * 16;
+    static constexpr int nbars = 2 * NS + 2 * NTS + 2;
+    static constexpr int off_flag = off_bars + nbars * 8;
+    static constexpr int total = off_flag + 16;
+};
+
+struct WaitCtx {
+    volatile int* abort_flag;
+    uint32_t* status;
+};
+
+__device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bits) { atomicOr(status, bits); }
+
+// Warp-collective bounded wait on an mbarrier phase. Returns false if the wait gave up (abort or timeout).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtx& ctx) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        const bool done = mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, done)) return true;
+        const bool stop = (*ctx.abort_flag != 0) || (global_timer_ns() - t0 > kWaitLimitNs);
+        if (__any_sync(0xffffffffu, stop)) {
+            if ((threadIdx.x & 31) == 0 && *ctx.abort_flag == 0) {
+                *ctx.abort_flag = 1;
+                raise_status(ctx.status, PKV_STATUS_TIMEOUT);
+            }
+            return false;
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag (used by the loader to drain its own copies before returning).
+__device__ __forceinline__ void warp_drain(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) {
+        if (__any_sync(0xffffffffu, global_timer_ns() - t0 > kWaitLimitNs)) return;
+    }
+}
+
+template <int G, int NCW, int NS, int NTS>
+__global__ void __launch_bounds__((NCW + 2) * 32, 2) decode_kernel(const DecodeParams p) {
+    using L = Layout<G, NCW, NS, NTS>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bars);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + NS;
+    uint64_t* tfull = bars + 2 * NS;
+    uint64_t* tempty = tfull + NTS;
+    uint64_t* cfull = tempty + NTS;
+    uint64_t* cempty = cfull + 1;
+    TaskSlot* slots = reinterpret_cast<TaskSlot*>(smem + L::off_slots);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_flag);
+    const WaitCtx ctx{abort_flag, &p.hdr->status};
+
+    // Zero the page ring once: slots past a row's last token are never copied and must hold finite values.
+    for (int i = threadIdx.x; i < NS * kStageBytes / 16; i += blockDim.x)
+        reinterpret_cast<int4*>(smem + L::off_stage)[i] = make_int4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < NTS; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], NCW + 1);
+        }
+        mbar_init(cfull, NCW);
+        mbar_init(cempty, NCW);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    const int Hq = p.Hq, Hkv = p.Hkv;
+
+    if (warp == NCW + 1) {
+        // ------------------------------------------------------------------ scheduler
+        const bool wq = p.variant == PKV_VARIANT_WORKQUEUE;
+        int count = p.num_tasks;
+        if (wq) count = min(*reinterpret_cast<volatile int32_t*>(&p.hdr->task_count), p.task_capacity);
+        const int per_row = Hkv * p.num_splits;
+        const __half* q = static_cast<const __half*>(p.q);
+        int tseq = 0;
+        for (int k = 0;; ++k) {
+            int t;
+            if (wq) {
+                int c = 0;
+                if (lane == 0) c = static_cast<int>(atomicAdd(&p.hdr->queue_head, 1u));
+                t = __shfl_sync(0xffffffffu, c, 0);
+            } else {
+                t = blockIdx.x + k * gridDim.x;
+            }
+            const int ts = tseq % NTS;
+            if (!warp_wait(&tempty[ts], ((tseq / NTS) & 1) ^ 1, ctx)) break;
+            TaskSlot* sl = &slots[ts];
+            if (t >= count) {
+                if (lane == 0) {
+                    sl->npages = -1;
+                    mbar_arrive(&tfull[ts]);
+                }
+                break;
+            }
+            int b, h, s, pb, pe;
+            if (wq) {
+                const pkv_task tk = p.tasks[t];
+                b = tk.row;
+                h = tk.head_split >> 16;
+                s = tk.head_split & 0xffff;
+                pb = tk.page_begin;
+                pe = tk.page_end;
+            } else {
+                b = t / per_row;
+                const int r = t - b * per_row;
+                h = r / p.num_splits;
+                s = r - h * p.num_splits;
+                pb = s * p.chunk_pages;
+                pe = pb + p.chunk_pages;
+            }
+            if (b < 0 || b >= p.B || h < 0 || h >= Hkv || pb < 0) {  // a task that is not from this plan
+                if (lane == 0) raise_status(ctx.status, PKV_STATUS_TASKS);
+                b = 0;
+                h = 0;
+                pb = pe = 0;
+            }
+            int len = p.seq_lens[b];
+            if (len < 0 || len > p.max_pages * kPageSize) {
+                if (lane == 0) raise_status(ctx.status, PKV_STATUS_BAD_LEN);
+                len = 0;
+            }
+            const int np_row = (len + kPageSize - 1) / kPageSize;
+            const int np = max(0, min(pe, np_row) - pb);
+            if (lane == 0) {
+                sl->b = b;
+                sl->h = h;
+                sl->s = s;
+                sl->task = t;
+                sl->page_begin = pb;
+                sl->npages = np;
+                sl->seq_len = len;
+            }
+            if (np > 0) {
+                if (lane == 0) mbar_arrive_expect_tx(&tfull[ts], G * kRowBytes);
+                __syncwarp();
+                if (lane < G)
+                    bulk_g2s(smem + L::off_q + ts * L::kQRowsBytes + lane * kSmemRow,
+                             q + ((size_t)b * Hq + (size_t)h * G + lane) * kHeadDim, kRowBytes, &tfull[ts]);
+            } else if (lane == 0) {
+                mbar_arrive(&tfull[ts]);
+            }
+            ++tseq;
+        }
+    } else if (warp == NCW) {
+        // ------------------------------------------------------------------ loader
+        const uint64_t pol = policy_evict_first();
+        const char* kpool = static_cast<const char*>(p.k_pool);
+        const char* vpool = static_cast<const char*>(p.v_pool);
+        const int row = lane & 15;
+        const char* pool = lane < 16 ? kpool : vpool;
+        const int dst_off = (lane < 16 ? 0 : kPageSize * kSmemRow) + row * kSmemRow;
+        int seq = 0, tseq = 0;
+        bool stop = false;
+        while (!stop) {
+            const int ts = tseq % NTS;
+            if (!warp_wait(&tfull[ts], (tseq / NTS) & 1, ctx)) break;
+            const TaskSlot sl = slots[ts];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[ts]);
+            if (sl.npages < 0) break;
+            const int32_t* bt = p.block_table + (size_t)sl.b * p.max_pages + sl.page_begin;
+            int ent_next = lane < sl.npages ? bt[lane] : 0;
+            for (int c0 = 0; c0 < sl.npages; c0 += 32) {
+                const int ent = ent_next;
+                if (c0 + 32 + lane < sl.npages) ent_next = bt[c0 + 32 + lane];
+                const int n = min(32, sl.npages - c0);
+                for (int i = 0; i < n; ++i) {
+                    const int phys = __shfl_sync(0xffffffffu, ent, i);
+                    const int pg = sl.page_begin + c0 + i;
+                    int nvalid = min(kPageSize, sl.seq_len - pg * kPageSize);
+                    if (phys < 0 || phys >= p.num_pages) {
+                        if (lane == 0) raise_status(ctx.status, PKV_STATUS_BAD_PAGE);
+                        nvalid = 0;
+                    }
+                    const int st = seq % NS;
+                    if (!warp_wait(&empty[st], ((seq / NS) & 1) ^ 1, ctx)) {
+                        stop = true;
+                        break;
+                    }
+                    if (lane == 0) {
+                        if (nvalid > 0)
+                            mbar_arrive_expect_tx(&full[st], nvalid * 2 * kRowBytes);
+                        else
+                            mbar_arrive(&full[st]);
+                    }
+                    __syncwarp();
+                    if (row < nvalid) {
+                        const char* src =
+                            pool + ((((size_t)phys * kPageSize + row) * Hkv + sl.h) * (size_t)kRowBytes);
+                        bulk_g2s_hint(smem + L::off_stage + st * kStageBytes + dst_off, src, kRowBytes, &full[st],
+                                      pol);
+                    }
+                    ++seq;
+                }
+                if (stop) break;
+            }
+            ++tseq;
+        }
+        // Wait for every copy this warp issued before the CTA may exit.
+        for (int j = max(0, seq - NS); j < seq; ++j) warp_drain(&full[j % NS], (j / NS) & 1);
+    } else {
+        // ------------------------------------------------------------------ consumers
+        const int w = warp;
+        const int g0 = lane >> 2;        // query head (row of the mma tile) this lane holds
+        const int tq = 2 * (lane & 3);   // first token column this lane holds in each 8-token half
+        const int mi = lane >> 3, mr = lane & 7;
+        // per-lane ldmatrix row offsets inside a stage (bytes)
+        const uint32_t k_lane = ((mi >> 1) * 8 + mr) * kSmemRow + (mi & 1) * 16;
+        const uint32_t v_lane = kPageSize * kSmemRow + ((mi & 1) * 8 + mr) * kSmemRow + (mi >> 1) * 16;
+        const uint32_t stage0 = smem_addr(smem + L::off_stage);
+        float* comb_o = reinterpret_cast<float*>(smem + L::off_comb);
+        float2* comb_ml = reinterpret_cast<float2*>(smem + L::off_comb_ml);
+        const float sl2 = p.scale_log2;
+        int seq = 0;
+        for (int tseq = 0;; ++tseq) {
+            const int ts = tseq % NTS;
+            if (!warp_wait(&tfull[ts], (tseq / NTS) & 1, ctx)) break;
+            const TaskSlot sl = slots[ts];
+            if (sl.npages < 0) break;
+            // Query fragments (A operand rows = query heads of the group; rows >= G are zero).
+            uint32_t qa[8][4];
+            {
+                const uint8_t* qs = smem + L::off_q + ts * L::kQRowsBytes;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int col = (ks * 16 + tq) * 2;
+                    qa[ks][0] = (g0 < G && sl.npages > 0) ? *reinterpret_cast<const uint32_t*>(qs + g0 * kSmemRow + col) : 0u;
+                    qa[ks][2] = (g0 < G && sl.npages > 0) ? *reinterpret_cast<const uint32_t*>(qs + g0 * kSmemRow + col + 16) : 0u;
+                    if constexpr (G > 8) {
+                        qa[ks][1] = (g0 + 8 < G && sl.npages > 0) ? *reinterpret_cast<const uint32_t*>(qs + (g0 + 8) * kSmemRow + col) : 0u;
+                        qa[ks][3] = (g0 + 8 < G && sl.npages > 0) ? *reinterpret_cast<const uint32_t*>(qs + (g0 + 8) * kSmemRow + col + 16) : 0u;
+                    } else {
+                        qa[ks][1] = 0u;
+                        qa[ks][3] = 0u;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[ts]);
+
+            float o[16][4];
+#pragma unroll
+            for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+            float m_lo = -INFINITY, l_lo = 0.f, m_hi = -INFINITY, l_hi = 0.f;
+            bool aborted = false;
+
+            for (int i = w; i < sl.npages; i += NCW) {
+                const int j = seq + i;
+                const int st = j % NS;
+                if (!warp_wait(&full[st], (j / NS) & 1, ctx)) {
+                    aborted = true;
+                    break;
+                }
+                const int nvalid = min(kPageSize, sl.seq_len - (sl.page_begin + i) * kPageSize);
+                const uint32_t sbase = stage0 + st * kStageBytes;
+                // S = Q K^T: two n8 tiles (tokens 0-7 and 8-15), k = head_dim in 8 steps
+                float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(sbase + k_lane + ks * 32, b0, b1, b2, b3);
+                    mma_16816(s0, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+                    mma_16816(s1, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+                }
+                // online softmax (base 2), row g0 and (G > 8) row g0 + 8
+                float x[4] = {s0[0] * sl2, s0[1] * sl2, s1[0] * sl2, s1[1] * sl2};
+                if (tq >= nvalid) x[0] = -INFINITY;
+                if (tq + 1 >= nvalid) x[1] = -INFINITY;
+                if (tq + 8 >= nvalid) x[2] = -INFINITY;
+                if (tq + 9 >= nvalid) x[3] = -INFINITY;
+                float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const float mn = fmaxf(m_lo, mx);
+                const float mu = mn == -INFINITY ? 0.f : mn;
+                const float alpha = fast_exp2(m_lo - mu);
+                float pr[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) pr[e] = fast_exp2(x[e] - mu);
+                l_lo = l_lo * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+                m_lo = mn;
+                uint32_t pa0 = pack_half2(pr[0], pr[1]);
+                uint32_t pa2 = pack_half2(pr[2], pr[3]);
+                uint32_t pa1 = 0u, pa3 = 0u;
+                float alpha_hi = 1.f;
+                if constexpr (G > 8) {
+                    float y[4] = {s0[2] * sl2, s0[3] * sl2, s1[2] * sl2, s1[3] * sl2};
+                    if (tq >= nvalid) y[0] = -INFINITY;
+                    if (tq + 1 >= nvalid) y[1] = -INFINITY;
+                    if (tq + 8 >= nvalid) y[2] = -INFINITY;
+                    if (tq + 9 >= nvalid) y[3] = -INFINITY;
+                    float my = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
+                    my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 1));
+                    my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 2));
+                    const float mnh = fmaxf(m_hi, my);
+                    const float muh = mnh == -INFINITY ? 0.f : mnh;
+                    alpha_hi = fast_exp2(m_hi - muh);
+                    float ph[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) ph[e] = fast_exp2(y[e] - muh);
+                    l_hi = l_hi * alpha_hi + ((ph[0] + ph[1]) + (ph[2] + ph[3]));
+                    m_hi = mnh;
+                    pa1 = pack_half2(ph[0], ph[1]);
+                    pa3 = pack_half2(ph[2], ph[3]);
+                }
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    o[n][0] *= alpha;
+                    o[n][1] *= alpha;
+                    if constexpr (G > 8) {
+                        o[n][2] *= alpha_hi;
+                        o[n][3] *= alpha_hi;
+                    }
+                }
+                // O += P V: 16 n8 tiles over head_dim, k = the 16 tokens
+#pragma unroll
+                for (int n2 = 0; n2 < 8; ++n2) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_trans(sbase + v_lane + n2 * 32, b0, b1, b2, b3);
+                    mma_16816(o[2 * n2], pa0, pa1, pa2, pa3, b0, b1);
+                    mma_16816(o[2 * n2 + 1], pa0, pa1, pa2, pa3, b2, b3);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st]);
+            }
+            if (aborted) break;
+            seq += sl.npages;
+
+            // ---- combine the NCW warps' states of this task
+            l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+            l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+            if constexpr (G > 8) {
+                l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+                l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+            }
+            if (!warp_wait(cempty, (tseq & 1) ^ 1, ctx)) break;
+            float* my_o = comb_o + w * G * kCombRow;
+            if (g0 < G) {
+#pragma unroll
+                for (int n = 0; n < 16; ++n)
+                    *reinterpret_cast<float2*>(my_o + g0 * kCombRow + n * 8 + tq) = make_float2(o[n][0], o[n][1]);
+                if ((lane & 3) == 0) comb_ml[w * G + g0] = make_float2(m_lo, l_lo);
+            }
+            if constexpr (G > 8) {
+                if (g0 + 8 < G) {
+#pragma unroll
+                    for (int n = 0; n < 16; ++n)
+                        *reinterpret_cast<float2*>(my_o + (g0 + 8) * kCombRow + n * 8 + tq) =
+                            make_float2(o[n][2], o[n][3]);
+                    if ((lane & 3) == 0) comb_ml[w * G + g0 + 8] = make_float2(m_hi, l_hi);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(cfull);
+            if (!warp_wait(cfull, tseq & 1, ctx)) break;
+            for (int g = w; g < G; g += NCW) {
+                float M = -INFINITY;
+#pragma unroll
+                for (int wi = 0; wi < NCW; ++wi) M = fmaxf(M, comb_ml[wi * G + g].x);
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+                float lsum = 0.f;
+                if (M != -INFINITY) {
+#pragma unroll
+                    for (int wi = 0; wi < NCW; ++wi) {
+                        const float2 ml = comb_ml[wi * G + g];
+                        const float f = fast_exp2(ml.x - M);
+                        lsum += f * ml.y;
+                        const float4 v = *reinterpret_cast<const float4*>(comb_o + (wi * G + g) * kCombRow + lane * 4);
+                        a.x += f * v.x;
+                        a.y += f * v.y;
+                        a.z += f * v.z;
+                        a.w += f * v.w;
+                    }
+                }
+                const int hq = sl.h * G + g;
+                if (p.variant == PKV_VARIANT_SINGLE) {
+                    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+                    uint2 pk;
+                    pk.x = pack_half2(a.x * inv, a.y * inv);
+                    pk.y = pack_half2(a.z * inv, a.w * inv);
+                    __half* out = static_cast<__half*>(p.out) + ((size_t)sl.b * Hq + hq) * kHeadDim;
+                    *reinterpret_cast<uint2*>(out + lane * 4) = pk;
+                } else {
+                    const size_t state = (size_t)sl.task * G + g;
+                    if (lane == 0)
+                        reinterpret_cast<float2*>(p.ml)[state] =
+                            make_float2(M == -INFINITY ? -INFINITY : M * kLn2, lsum);
+                    reinterpret_cast<float4*>(p.acc + state * kHeadDim)[lane] = a;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(cempty);
+        }
+    }
+}
+
+constexpr int kNCW = 4;
+constexpr int kNS = 8;
+constexpr int kNTS = 4;
+
+template <int G>
+int launch_g(const DecodeParams& p, int grid, cudaStream_t stream) {
+    using L = Layout<G, kNCW, kNS, kNTS>;
+    static int configured_mask = 0;  // one bit per device ordinal (< 32)
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 32 && !(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<G, kNCW, kNS, kNTS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::total);
+        if (e != cudaSuccess) return e;
+        __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_ACQ_REL);
+    }
+    decode_kernel<G, kNCW, kNS, kNTS><<<grid, (kNCW + 2) * 32, L::total, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int decode_smem_bytes(int group) {
+    switch (group) {
+        case 1: return Layout<1, kNCW, kNS, kNTS>::total;
+        case 2: return Layout<2, kNCW, kNS, kNTS>::total;
+        case 4: return Layout<4, kNCW, kNS, kNTS>::total;
+        case 8: return Layout<8, kNCW, kNS, kNTS>::total;
+        case 16: return Layout<16, kNCW, kNS, kNTS>::total;
+        default: return 0;
+    }
+}
+
+int launch_decode(const DecodeParams& p, int group, int grid, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (group) {
+        case 1: return launch_g<1>(p, grid, s);
+        case 2: return launch_g<2>(p, grid, s);
+        case 4: return launch_g<4>(p, grid, s);
+        case 8: return launch_g<8>(p, grid, s);
+        case 16: return launch_g<16>(p, grid, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pkv

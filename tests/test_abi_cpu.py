@@ -1,0 +1,124 @@
+"""The C-ABI library on the CPU: it loads, exports every declared symbol, and its host-only logic is right.
+
+No call here touches the GPU: only pkv_version, pkv_strerror, pkv_check_problem, pkv_policy_default, pkv_plan,
+pkv_plan_fixed and pkv_plan_launches run; they are host code.
+"""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import serving_paged_gqa_gb300 as pkv
+from serving_paged_gqa_gb300 import _lib
+from workloads import make_trace
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from serving_paged_gqa_gb300 import build
+
+    build.build()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:int|void|const char\*)\s+(pkv_\w+)\s*\(", text, re.M)))
+
+
+def test_exports_every_declared_symbol():
+    lib = ctypes.CDLL(_lib.LIB_PATH)
+    names = _declared()
+    assert len(names) >= 13
+    assert sorted(_lib.EXPORTS) == names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_errors():
+    assert pkv.pkv_version() == 1
+    assert "null" in pkv.pkv_strerror(-3)
+    assert pkv.pkv_strerror(0) == "ok"
+
+
+def _problem(B=8, Hq=32, Hkv=8, d=128, ps=16, num_pages=1 << 16, max_pages=2100):
+    return pkv.make_problem(B, Hq, Hkv, d, ps, num_pages, max_pages)
+
+
+def test_check_problem():
+    assert pkv.pkv_check_problem(_problem()) == 0
+    assert pkv.pkv_check_problem(_problem(d=64)) == -2
+    assert pkv.pkv_check_problem(_problem(ps=32)) == -2
+    assert pkv.pkv_check_problem(_problem(Hq=32, Hkv=6)) == -2  # Hq % Hkv != 0
+    assert pkv.pkv_check_problem(_problem(Hq=96, Hkv=2)) == -2  # G = 48 unsupported
+    assert pkv.pkv_check_problem(_problem(B=-1)) == -1
+    assert pkv.pkv_check_problem(_problem(B=5000)) == -2
+
+
+def test_plan_fixed_counts_match_oracle_worklist():
+    tr = make_trace("b8_bimodal", 5, steps=3)
+    lens = tr.seq_lens(2)
+    pr = _problem(max_pages=tr.max_pages)
+    for c in (1, 4, 32, 100):
+        wq = pkv.pkv_plan_fixed(pr, lens, 152, pkv.PKV_VARIANT_WORKQUEUE, c)
+        assert wq.num_tasks == len(oracle.worklist(lens, 16, 8, c))
+        assert wq.task_capacity == wq.num_tasks and wq.state_capacity == 4 * wq.num_tasks
+        sp = pkv.pkv_plan_fixed(pr, lens, 152, pkv.PKV_VARIANT_SPLIT, c)
+        S = max(-(-(-(-int(L) // 16)) // c) for L in lens)
+        assert sp.num_splits == S and sp.num_tasks == 8 * 8 * S
+        for pl in (wq, sp):
+            assert pl.grid_ctas == min(pl.num_tasks, 2 * 152)
+            offs = [pl.off_row_off, pl.off_row_splits, pl.off_tasks, pl.off_ml, pl.off_acc, pl.ws_bytes]
+            assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+            assert pl.off_acc + 4 * 128 * pl.state_capacity <= pl.ws_bytes
+            assert abs(pl.kv_bytes - (4096 * int(lens.sum()) + 16384 * 8)) < 1
+    single = pkv.pkv_plan_fixed(pr, lens, 152, pkv.PKV_VARIANT_SINGLE)
+    assert single.num_tasks == 64 and single.num_splits == 1 and single.state_capacity == 0
+    assert pkv.pkv_plan_launches(single) == 1
+
+
+def test_plan_rejects_bad_input():
+    pr = _problem(B=2, max_pages=4)
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_plan_fixed(pr, [10, 65], 152, pkv.PKV_VARIANT_SPLIT, 2)  # 65 > 4 pages * 16
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_plan_fixed(pr, [10, 20], 152, pkv.PKV_VARIANT_SPLIT, 0)
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_plan_fixed(pr, [10, 20], 0, pkv.PKV_VARIANT_SPLIT, 1)
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_plan_fixed(pr, [10, 20], 152, 7, 1)
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_plan(pr, [-1, 20], 152)
+
+
+def test_plan_picks_the_model_minimum():
+    """pkv_plan's choice has the lowest predicted time among all fixed plans it could have made."""
+    for name, seed in (("b1_bucketed", 5), ("b8_bimodal", 6), ("b4_bimodal", 7), ("b8_zipf", 8), ("tiny", 0)):
+        tr = make_trace(name, seed, steps=1)
+        lens = tr.seq_lens(0)
+        pr = _problem(B=tr.batch, max_pages=tr.max_pages, num_pages=tr.num_pages)
+        best = pkv.pkv_plan(pr, lens, 152)
+        pmax = int(tr.pages(0).max())
+        cands = [pkv.pkv_plan_fixed(pr, lens, 152, pkv.PKV_VARIANT_SINGLE)]
+        for v in (pkv.PKV_VARIANT_SPLIT, pkv.PKV_VARIANT_WORKQUEUE):
+            for c in range(max(1, -(-pmax // 256)), pmax + 1):
+                cands.append(pkv.pkv_plan_fixed(pr, lens, 152, v, c))
+        low = min(c.predicted_us for c in cands)
+        # the planner searches a subset of split sizes; it may not beat the full sweep, and must be close to it
+        assert best.predicted_us >= low - 1e-9
+        assert best.predicted_us <= low * 1.15
+
+
+def test_empty_batch_and_empty_rows_plan():
+    pr = _problem(B=3, max_pages=8)
+    pl = pkv.pkv_plan_fixed(pr, [0, 0, 0], 152, pkv.PKV_VARIANT_WORKQUEUE, 2)
+    assert pl.num_tasks == 0
+    pl = pkv.pkv_plan_fixed(pr, [0, 17, 0], 152, pkv.PKV_VARIANT_WORKQUEUE, 1)
+    assert pl.num_tasks == 8 * 2
+    pl = pkv.pkv_plan(_problem(B=0, max_pages=1), np.zeros(0, np.int32), 152)
+    assert pl.num_tasks == 0

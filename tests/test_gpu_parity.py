@@ -1,0 +1,264 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the same seeded inputs.
+
+Worklists must be bit-exact; outputs within 2e-3 absolute + 1e-2 relative of the oracle, elementwise.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import serving_paged_gqa_gb300 as pkv
+from workloads import make_trace, normal_fp16, rng_for
+
+from gpu_harness import Step, assert_close, read_worklist
+
+pytestmark = pytest.mark.gpu
+
+SINGLE, SPLIT, WQ = pkv.PKV_VARIANT_SINGLE, pkv.PKV_VARIANT_SPLIT, pkv.PKV_VARIANT_WORKQUEUE
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+# ----------------------------------------------------------------------------------------------- worklist builder
+def _check_worklist(step, chunk):
+    plan = step.plan(WQ, chunk)
+    ws = pkv.alloc_workspace(plan.ws_bytes)
+    pkv.pkv_build_worklist(plan, step.problem, step.lens, ws)
+    got, row_off, row_splits, head = read_worklist(plan, ws)
+    want = oracle.worklist(step.lens_host, 16, step.tr.hkv, chunk)
+    assert got.shape == want.shape and np.array_equal(got, want), f"worklist differs (c={chunk})"
+    P = (step.lens_host.astype(np.int64) + 15) // 16
+    S = (P + chunk - 1) // chunk
+    assert np.array_equal(row_splits, S)
+    assert np.array_equal(row_off, np.concatenate([[0], np.cumsum(step.tr.hkv * S)[:-1]]))
+    assert head == 0 and pkv.pkv_read_status(ws) == 0
+
+
+@pytest.mark.parametrize("name,seed,t", [
+    ("tiny", 0, 0), ("b1_bucketed", 5, 0), ("b1_bucketed", 6, 63), ("b8_bimodal", 5, 0), ("b8_bimodal", 9, 63),
+    ("b8_uniform", 5, 31), ("b8_zipf", 7, 63), ("b4_bimodal", 5, 10), ("stress", 5, 0),
+])
+def test_worklist_bit_exact_configs(name, seed, t):
+    tr = make_trace(name, seed, steps=max(t + 1, 1))
+    step = Step(tr, t, poison=False)
+    for chunk in (1, 3, 8, 32, 64, 1000):
+        _check_worklist(step, chunk)
+
+
+class _Lens:
+    """A step built from explicit lengths (edge cases)."""
+
+    def __init__(self, lens, hkv=8, hq=32, seed=0, extra=5):
+        from workloads.traces import Trace
+
+        lens = np.asarray(lens, dtype=np.int64)
+        r = rng_for(seed, 4242)
+        P = (lens + 15) // 16
+        n = int(P.sum())
+        num_pages = n + extra
+        perm = r.permutation(num_pages)
+        max_pages = max(int(P.max()), 1)
+        table = np.full((len(lens), max_pages), -1, dtype=np.int32)
+        used, rows, logical = [], [], []
+        k = 0
+        for b, p in enumerate(P):
+            for j in range(int(p)):
+                table[b, j] = perm[k]
+                used.append(perm[k])
+                rows.append(b)
+                logical.append(j)
+                k += 1
+        self.trace = Trace(name="edge", seed=seed, batch=len(lens), steps=1, num_pages=num_pages, start=lens,
+                           table=table, used_pages=np.array(used, dtype=np.int64),
+                           page_row=np.array(rows, dtype=np.int64), page_logical=np.array(logical, dtype=np.int64),
+                           hq=hq, hkv=hkv)
+
+
+def test_worklist_edge_lengths():
+    step = Step(_Lens([1, 16, 17, 0, 32, 33, 255, 0]).trace, 0)
+    for chunk in (1, 2, 3, 100):
+        _check_worklist(step, chunk)
+    empty = Step(_Lens([0, 0, 0]).trace, 0)
+    _check_worklist(empty, 4)
+
+
+# ------------------------------------------------------------------------------------------------- decode + merge
+@pytest.mark.parametrize("seed", range(10))
+def test_tiny_all_schedules(seed):
+    step = Step(make_trace("tiny", seed), 0)
+    ref = step.reference()
+    outs = []
+    for variant, chunk in ((SPLIT, 8), (WQ, 8), (SINGLE, 1), (SPLIT, 3), (WQ, 1), (SPLIT, 32), (None, 1)):
+        out, _, status = step.run(step.plan(variant, chunk))
+        assert status == 0
+        assert_close(out, ref, f"tiny seed {seed} variant {variant} c={chunk}")
+        outs.append(out.float())
+    for o in outs[1:]:  # schedules agree with each other to fp32 round-off plus one fp16 rounding
+        assert (o - outs[0]).abs().max().item() < 2e-3
+
+
+@pytest.mark.parametrize("name,seed,steps", [
+    ("b1_bucketed", 5, (0, 63)), ("b1_bucketed", 8, (17,)), ("b8_bimodal", 5, (0, 63)), ("b8_uniform", 6, (40,)),
+    ("b8_zipf", 7, (0, 63)), ("b4_bimodal", 5, (5,)),
+])
+def test_traces_policy_and_forced_schedules(name, seed, steps):
+    tr = make_trace(name, seed)
+    for t in steps:
+        step = Step(tr, t)
+        ref = step.reference()
+        plans = [step.plan()]
+        pmax = int(tr.pages(t).max())
+        for S in (8, 64):
+            plans.append(step.plan(SPLIT, -(-pmax // S)))
+        plans.append(step.plan(WQ, 32))
+        if tr.batch > 1:
+            plans.append(step.plan(SINGLE))
+        for plan in plans:
+            out, _, status = step.run(plan)
+            assert status == 0, status
+            assert_close(out, ref, f"{name} seed {seed} step {t} {plan.describe()}")
+
+
+def test_stress_sampled_pairs():
+    tr = make_trace("stress", 5, steps=1)
+    step = Step(tr, 0)
+    r = rng_for(5, 777)
+    pairs = np.stack([np.arange(tr.batch), r.integers(0, tr.hq, tr.batch)], axis=1)
+    ref = step.reference(pairs)
+    for plan in (step.plan(), step.plan(WQ, 64)):
+        out, _, status = step.run(plan)
+        assert status == 0
+        got = out[torch.from_numpy(pairs[:, 0]), torch.from_numpy(pairs[:, 1])]
+        assert_close(got, ref, f"stress {plan.describe()}")
+
+
+def test_edge_lengths_and_empty_rows():
+    step = Step(_Lens([1, 15, 16, 17, 0, 31, 32, 33, 1000, 0]).trace, 0)
+    ref = step.reference()
+    for variant, chunk in ((SINGLE, 1), (SPLIT, 1), (SPLIT, 5), (WQ, 1), (WQ, 2), (None, 1)):
+        out, _, status = step.run(step.plan(variant, chunk))
+        assert status == 0
+        assert_close(out, ref, f"edge {variant} {chunk}")
+        assert not out[4].any() and not out[9].any()  # empty rows give 0
+    allempty = Step(_Lens([0, 0]).trace, 0)
+    for variant in (SINGLE, SPLIT, WQ):
+        out, _, status = allempty.run(allempty.plan(variant, 2))
+        assert status == 0
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (16, 2), (16, 1), (32, 2)])
+def test_group_sizes(hq, hkv):
+    step = Step(_Lens([40, 300, 17], hkv=hkv, hq=hq, seed=hq * 10 + hkv).trace, 0)
+    ref = step.reference()
+    for variant, chunk in ((SINGLE, 1), (SPLIT, 4), (WQ, 2)):
+        out, _, status = step.run(step.plan(variant, chunk))
+        assert status == 0
+        assert_close(out, ref, f"G={hq // hkv} variant {variant}")
+
+
+def test_partial_states_match_oracle_split_states():
+    step = Step(make_trace("tiny", 2), 0)
+    chunk = 8
+    plan = step.plan(SPLIT, chunk)
+    _, ws, status = step.run(plan)
+    assert status == 0
+    ml = ws[plan.off_ml:plan.off_ml + 8 * plan.state_capacity].view(torch.float32).cpu().numpy().reshape(-1, 2)
+    acc = ws[plan.off_acc:plan.off_acc + 512 * plan.state_capacity].view(torch.float32).cpu().numpy()
+    acc = acc.reshape(-1, 128)
+    kp, vp = step.tr.host_pools()
+    S, G = plan.num_splits, plan.group
+    for hq in (0, 5, 31):
+        h, g = hq // G, hq % G
+        ranges = [(s * chunk * 16, (s + 1) * chunk * 16) for s in range(S)]
+        m, l, a = oracle.split_states(step.q_host, kp, vp, step.bt_host, step.lens_host, 0, hq, ranges)
+        for s in range(S):
+            st = (h * S + s) * G + g
+            assert abs(ml[st, 0] - m[s]) < 1e-3
+            assert abs(ml[st, 1] - l[s]) <= 1e-3 * l[s]
+            assert np.max(np.abs(acc[st] / ml[st, 1] - a[s] / l[s])) < 2e-3
+
+
+def test_rect_empty_splits_write_neutral_states():
+    step = Step(_Lens([16, 200]).trace, 0)
+    plan = step.plan(SPLIT, 1)  # row 0 has 1 split, row 1 has 13: row 0's splits 1..12 are empty
+    _, ws, status = step.run(plan)
+    assert status == 0
+    ml = ws[plan.off_ml:plan.off_ml + 8 * plan.state_capacity].view(torch.float32).cpu().numpy().reshape(-1, 2)
+    acc = ws[plan.off_acc:plan.off_acc + 512 * plan.state_capacity].view(torch.float32).cpu().numpy()
+    acc = acc.reshape(-1, 128)
+    S, G = plan.num_splits, plan.group
+    for h in range(8):
+        for s in range(1, S):
+            for g in range(G):
+                st = ((0 * 8 + h) * S + s) * G + g
+                assert ml[st, 0] == -np.inf and ml[st, 1] == 0 and not acc[st].any()
+
+
+def test_workqueue_repeated_calls_reuse_workspace():
+    tr = make_trace("b8_bimodal", 6, steps=3)
+    ws = None
+    for t in range(3):
+        step = Step(tr, t)
+        plan = step.plan(WQ, 16)
+        if ws is None:
+            ws = pkv.alloc_workspace(plan.ws_bytes * 2)
+        out, _, status = step.run(plan, ws)
+        assert status == 0
+        assert_close(out, step.reference(), f"repeat step {t}")
+
+
+def test_python_decode_api():
+    step = Step(make_trace("b8_zipf", 9, steps=1), 0)
+    out = pkv.decode(step.q, step.k, step.v, step.bt, step.lens, seq_lens_host=step.lens_host)
+    torch.cuda.synchronize()
+    assert_close(out, step.reference(), "pkv.decode")
+
+
+# ------------------------------------------------------------------------------------------- device-side checks
+def test_bad_block_table_entry_sets_status():
+    step = Step(make_trace("tiny", 1), 0, poison=False)
+    step.bt[0, 3] = step.tr.num_pages + 5
+    for variant in (SPLIT, WQ, SINGLE):
+        out, ws, status = step.run(step.plan(variant, 8))
+        assert status & pkv.PKV_STATUS_BAD_PAGE
+        assert pkv.pkv_read_status(ws) == 0  # reading clears it
+
+
+def test_bad_length_sets_status():
+    step = Step(make_trace("tiny", 1), 0, poison=False)
+    plan = step.plan(WQ, 8)
+    step.lens[0] = step.tr.max_pages * 16 + 1
+    out, ws, status = step.run(plan)
+    assert status & pkv.PKV_STATUS_BAD_LEN
+    plan = step.plan(SPLIT, 8)
+    out, ws, status = step.run(plan)
+    assert status & pkv.PKV_STATUS_BAD_LEN
+
+
+def test_api_rejects_bad_arguments_before_launch():
+    step = Step(make_trace("tiny", 1), 0)
+    plan = step.plan(SPLIT, 8)
+    ws = pkv.alloc_workspace(plan.ws_bytes)
+    out = torch.empty_like(step.q)
+    small = pkv.alloc_workspace(plan.ws_bytes // 2)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_decode_step(plan, step.problem, step.q, step.k, step.v, step.bt, step.lens, step.scale, small, out)
+    assert e.value.code == -4
+    other = pkv.make_problem(1, 32, 8, 128, 16, 65, 32)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_decode_step(plan, other, step.q, step.k, step.v, step.bt, step.lens, step.scale, ws, out)
+    assert e.value.code == -1
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_build_worklist(plan, step.problem, step.lens, ws)  # a split plan has no worklist
+    assert e.value.code == -1
+    mis = torch.empty(step.q.numel() + 8, dtype=torch.float16, device="cuda")[1:1 + step.q.numel()].view_as(step.q)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_decode_step(plan, step.problem, mis, step.k, step.v, step.bt, step.lens, step.scale, ws, out)
+    assert e.value.code == -5

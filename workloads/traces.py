@@ -14,6 +14,7 @@ seed gives the same trace on any machine. Nothing here computes attention.
 from __future__ import annotations
 
 import math
+import mmap
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -47,6 +48,21 @@ def normal_fp16(rng: np.random.Generator, shape) -> np.ndarray:
     n = int(np.prod(shape, dtype=np.int64))
     idx = np.frombuffer(rng.bytes(2 * n), dtype=np.uint16)
     return _normal_table()[idx].reshape(shape)
+
+
+def lazy_zeros(shape, dtype) -> np.ndarray:
+    """A zero-filled array whose memory is committed only where written (anonymous mmap, no huge pages), so a
+    GB-sized page pool with a few thousand pages filled costs only those pages."""
+    nbytes = int(np.prod(shape, dtype=np.int64)) * np.dtype(dtype).itemsize
+    if nbytes < (1 << 22):
+        return np.zeros(shape, dtype=dtype)
+    buf = mmap.mmap(-1, nbytes)
+    if hasattr(mmap, "MADV_NOHUGEPAGE"):
+        try:
+            buf.madvise(mmap.MADV_NOHUGEPAGE)
+        except OSError:
+            pass
+    return np.frombuffer(buf, dtype=dtype).reshape(shape)
 
 
 def zipf_lengths(rng: np.random.Generator, n: int, s: float = 1.1, kmax: int = 128, unit: int = 256) -> np.ndarray:
@@ -184,8 +200,8 @@ class Trace:
         """
         k, v = self._contents()
         shape = (self.num_pages, self.ps, self.hkv, self.d)
-        kp = np.zeros(shape, dtype=np.float16)
-        vp = np.zeros(shape, dtype=np.float16)
+        kp = lazy_zeros(shape, np.float16)
+        vp = lazy_zeros(shape, np.float16)
         kp[self.used_pages] = k
         vp[self.used_pages] = v
         return kp, vp
