@@ -53,6 +53,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--pool-pages", type=int, default=0, help="override the page-pool size (small profiling runs)")
     ap.add_argument("--reference-budget", type=float, default=120.0, help="seconds for the reference arm's steps")
     return ap.parse_args(argv)
 
@@ -146,7 +147,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------------------ workload
-def build_workload(config: str, seeds, dev):
+def build_workload(config: str, seeds, dev, pool_pages: int = 0):
     """Device tensors for every step of every trace: pools with all pages a trace will use, per-step q, block
     table and lengths. Returns a list of step records."""
     import torch
@@ -156,7 +157,7 @@ def build_workload(config: str, seeds, dev):
     steps = []
     traces = []
     for seed in seeds:
-        tr = make_trace(config, seed)
+        tr = make_trace(config, seed, pool_pages=pool_pages or None)
         ps, hkv, d = tr.ps, tr.hkv, tr.d
         k = torch.empty((tr.num_pages, ps, hkv, d), dtype=torch.float16, device=dev)
         v = torch.empty((tr.num_pages, ps, hkv, d), dtype=torch.float16, device=dev)
@@ -280,7 +281,7 @@ def run_ours(args):
     import serving_paged_gqa_gb300 as pkv
 
     seeds = [int(s) for s in args.seeds.split(",")]
-    traces, steps = build_workload(args.config, seeds, dev)
+    traces, steps = build_workload(args.config, seeds, dev, args.pool_pages)
     tr0 = traces[0][0]
     B, Hq, Hkv, d = tr0.batch, tr0.hq, tr0.hkv, tr0.d
     sms = torch.cuda.get_device_properties(dev).multi_processor_count

@@ -1,8 +1,10 @@
 // C-ABI entry points of libpkv.so: argument validation and kernel launches (see include/pkv.h).
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 
 #include "pkv_internal.h"
 
@@ -34,6 +36,63 @@ T* at(void* ws, int64_t off) {
 }
 
 int cuda_rc(int e) { return e == cudaSuccess ? PKV_OK : PKV_E_CUDA; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// TMA descriptor of a K or V pool [num_pages][page_size][Hkv][d] seen as the 3-D tensor (d, Hkv, num_pages *
+// page_size) with box (64, 1, page_size) and 128-byte swizzle. Descriptors are cached by (device, pointer, shape).
+int pool_tensor_map(const void* pool, int num_pages, int hkv, CUtensorMap* out) {
+    struct Entry {
+        const void* ptr;
+        int num_pages, hkv, dev;
+        CUtensorMap map;
+    };
+    static std::mutex mu;
+    static Entry cache[32];
+    static int used = 0, next = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_E_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i) {
+            const Entry& e = cache[i];
+            if (e.ptr == pool && e.num_pages == num_pages && e.hkv == hkv && e.dev == dev) {
+                *out = e.map;
+                return PKV_OK;
+            }
+        }
+    }
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return PKV_E_CUDA;
+    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv, (cuuint64_t)num_pages * kPageSize};
+    const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)hkv * kRowBytes};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)kPageSize};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUtensorMap m;
+    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return PKV_E_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    Entry& e = cache[next];
+    e = Entry{pool, num_pages, hkv, dev, m};
+    next = (next + 1) % 32;
+    used = std::max(used, next == 0 ? 32 : next);
+    *out = m;
+    return PKV_OK;
+}
 
 }  // namespace
 
@@ -95,6 +154,11 @@ extern "C" int pkv_decode(const pkv_plan_t* plan, const pkv_problem* pr, const v
     if (!(scale == scale)) return PKV_E_INVAL;
     if (plan->num_tasks == 0) return PKV_OK;
     DecodeParams p{};
+    if (pr->num_pages > 0) {
+        rc = pool_tensor_map(k_pool, pr->num_pages, pr->num_kv_heads, &p.tmap_k);
+        if (rc == PKV_OK) rc = pool_tensor_map(v_pool, pr->num_pages, pr->num_kv_heads, &p.tmap_v);
+        if (rc != PKV_OK) return rc;
+    }
     p.q = q;
     p.k_pool = k_pool;
     p.v_pool = v_pool;

@@ -6,12 +6,13 @@
 // tile; gist.science technical summary, "Methodologie" 1: native block-table execution, sequence splitting into
 // partial online-softmax states, row-local bounds with neutral states for empty splits, compact workqueue).
 //
-// CTA layout (one or two CTAs per SM, persistent over tasks):
+// CTA layout (two CTAs per SM, persistent over tasks):
 //   warp NCW+1  scheduler: claims tasks (atomic queue head for the workqueue, a static stride otherwise), reads the
 //               row length, publishes the task in a shared-memory slot and bulk-copies the G query rows into it;
-//   warp NCW    loader: walks the task's block-table entries (32 per load, prefetched one chunk ahead) and, per
-//               page, has 32 lanes issue one 256-byte bulk copy each (16 K rows + 16 V rows of KV head h) into a
-//               ring stage, completion counted in bytes on the stage's mbarrier;
+//   warp NCW    loader: walks the task's block-table entries (32 per load, prefetched one chunk ahead); per page
+//               one elected lane issues four 3-D TMA tensor copies (K and V of KV head h, each as two 64-column
+//               boxes of the page's 16 token rows, 128-byte swizzled) into a ring stage; completion is counted in
+//               bytes on the stage's mbarrier;
 //   warps 0..NCW-1 consumers: page i of a task goes to warp i % NCW. Per page: S = Q K^T on mma.sync m16n8k16
 //               (rows = the G query heads, columns = the 16 tokens), masking of slots past the row length, online
 //               softmax in base 2 in registers with quad shuffles, O += P V on mma.sync. At the end of the task the
@@ -27,10 +28,10 @@
 namespace pkv {
 namespace {
 
-constexpr int kSmemRow = kRowBytes + 16;           // padded row: ldmatrix over 8 rows hits 8 distinct bank groups
-constexpr int kStageBytes = 2 * kPageSize * kSmemRow;
-constexpr int kCombRow = kHeadDim + 8;             // floats per combined row (padding against bank conflicts)
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+constexpr int kBoxBytes = kPageSize * 128;   // one TMA box: 16 token rows x 64 fp16 columns (128 B, swizzled)
+constexpr int kStageBytes = 4 * kBoxBytes;   // K columns 0-63, K 64-127, V 0-63, V 64-127
+constexpr int kCombRow = kHeadDim + 8;       // floats per combined row (padding against bank conflicts)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct TaskSlot {
@@ -39,8 +40,8 @@ struct TaskSlot {
 
 template <int G, int NCW, int NS, int NTS>
 struct Layout {
-    static constexpr int kQRowsBytes = ((G * kSmemRow + 127) / 128) * 128;
-    static constexpr int off_stage = 0;
+    static constexpr int kQRowsBytes = ((G * kRowBytes + 127) / 128) * 128;
+    static constexpr int off_stage = 0;  // 1024-byte aligned (128-byte swizzle atom)
     static constexpr int off_q = off_stage + NS * kStageBytes;
     static constexpr int off_comb = off_q + NTS * kQRowsBytes;
     static constexpr int comb_o_floats = NCW * G * kCombRow;
@@ -49,7 +50,8 @@ struct Layout {
     static constexpr int off_bars = ((off_slots + NTS * (int)sizeof(TaskSlot) + 15) / 16) * 16;
     static constexpr int nbars = 2 * NS + 2 * NTS + 2;
     static constexpr int off_flag = off_bars + nbars * 8;
-    static constexpr int total = off_flag + 16;
+    static constexpr int used = off_flag + 16;
+    static constexpr int total = used + 1024;  // slack to align the base to 1024 bytes
 };
 
 struct WaitCtx {
@@ -60,35 +62,53 @@ struct WaitCtx {
 __device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bits) { atomicOr(status, bits); }
 
 // Warp-collective bounded wait on an mbarrier phase. Returns false if the wait gave up (abort or timeout).
+// try_wait suspends the thread until the phase completes or a short hardware time slice ends; the abort flag and
+// the global timer are consulted only every kPollEvery slices.
+constexpr uint32_t kPollEvery = 256;
+
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtx& ctx) {
     if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        const bool done = mbar_try_wait(bar, parity);
-        if (__all_sync(0xffffffffu, done)) return true;
-        const bool stop = (*ctx.abort_flag != 0) || (global_timer_ns() - t0 > kWaitLimitNs);
-        if (__any_sync(0xffffffffu, stop)) {
-            if ((threadIdx.x & 31) == 0 && *ctx.abort_flag == 0) {
-                *ctx.abort_flag = 1;
-                raise_status(ctx.status, PKV_STATUS_TIMEOUT);
+    uint64_t t0 = 0;
+    for (uint32_t it = 1;; ++it) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        if (it % kPollEvery == 0) {
+            const uint64_t now = global_timer_ns();
+            if (t0 == 0) t0 = now;
+            const bool stop = (*ctx.abort_flag != 0) || (now - t0 > kWaitLimitNs);
+            if (__any_sync(0xffffffffu, stop)) {
+                if ((threadIdx.x & 31) == 0 && *ctx.abort_flag == 0) {
+                    *ctx.abort_flag = 1;
+                    raise_status(ctx.status, PKV_STATUS_TIMEOUT);
+                }
+                return false;
             }
-            return false;
         }
     }
 }
 
 // Bounded wait that ignores the abort flag (used by the loader to drain its own copies before returning).
 __device__ __forceinline__ void warp_drain(uint64_t* bar, uint32_t parity) {
-    const uint64_t t0 = global_timer_ns();
-    while (!__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) {
-        if (__any_sync(0xffffffffu, global_timer_ns() - t0 > kWaitLimitNs)) return;
+    uint64_t t0 = 0;
+    for (uint32_t it = 1; !__all_sync(0xffffffffu, mbar_try_wait(bar, parity)); ++it) {
+        if (it % kPollEvery == 0) {
+            const uint64_t now = global_timer_ns();
+            if (t0 == 0) t0 = now;
+            if (__any_sync(0xffffffffu, now - t0 > kWaitLimitNs)) return;
+        }
     }
 }
 
+// Byte offset of the 16-byte chunk `chunk` (0..7) of token row `row` inside a 128-byte-swizzled box: the TMA
+// stores chunk c of row r at position c ^ (r % 8) of the row's 128-byte line.
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+    return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
 template <int G, int NCW, int NS, int NTS>
-__global__ void __launch_bounds__((NCW + 2) * 32, 2) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__((NCW + 2) * 32, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
     using L = Layout<G, NCW, NS, NTS>;
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -103,7 +123,7 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 2) decode_kernel(const DecodeP
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_flag);
     const WaitCtx ctx{abort_flag, &p.hdr->status};
 
-    // Zero the page ring once: slots past a row's last token are never copied and must hold finite values.
+    // Zero the page ring once, so a stage never holds uninitialised bits.
     for (int i = threadIdx.x; i < NS * kStageBytes / 16; i += blockDim.x)
         reinterpret_cast<int4*>(smem + L::off_stage)[i] = make_int4(0, 0, 0, 0);
     fence_proxy_async_smem();
@@ -189,26 +209,20 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 2) decode_kernel(const DecodeP
                 sl->page_begin = pb;
                 sl->npages = np;
                 sl->seq_len = len;
+                if (np > 0) {  // the G query rows of this KV head are contiguous in q
+                    mbar_arrive_expect_tx(&tfull[ts], G * kRowBytes);
+                    bulk_g2s(smem + L::off_q + ts * L::kQRowsBytes, q + ((size_t)b * Hq + (size_t)h * G) * kHeadDim,
+                             G * kRowBytes, &tfull[ts]);
+                } else {
+                    mbar_arrive(&tfull[ts]);
+                }
             }
-            if (np > 0) {
-                if (lane == 0) mbar_arrive_expect_tx(&tfull[ts], G * kRowBytes);
-                __syncwarp();
-                if (lane < G)
-                    bulk_g2s(smem + L::off_q + ts * L::kQRowsBytes + lane * kSmemRow,
-                             q + ((size_t)b * Hq + (size_t)h * G + lane) * kHeadDim, kRowBytes, &tfull[ts]);
-            } else if (lane == 0) {
-                mbar_arrive(&tfull[ts]);
-            }
+            __syncwarp();
             ++tseq;
         }
     } else if (warp == NCW) {
         // ------------------------------------------------------------------ loader
         const uint64_t pol = policy_evict_first();
-        const char* kpool = static_cast<const char*>(p.k_pool);
-        const char* vpool = static_cast<const char*>(p.v_pool);
-        const int row = lane & 15;
-        const char* pool = lane < 16 ? kpool : vpool;
-        const int dst_off = (lane < 16 ? 0 : kPageSize * kSmemRow) + row * kSmemRow;
         int seq = 0, tseq = 0;
         bool stop = false;
         while (!stop) {
@@ -226,30 +240,27 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 2) decode_kernel(const DecodeP
                 const int n = min(32, sl.npages - c0);
                 for (int i = 0; i < n; ++i) {
                     const int phys = __shfl_sync(0xffffffffu, ent, i);
-                    const int pg = sl.page_begin + c0 + i;
-                    int nvalid = min(kPageSize, sl.seq_len - pg * kPageSize);
-                    if (phys < 0 || phys >= p.num_pages) {
-                        if (lane == 0) raise_status(ctx.status, PKV_STATUS_BAD_PAGE);
-                        nvalid = 0;
-                    }
+                    const bool ok = phys >= 0 && phys < p.num_pages;
+                    if (!ok && lane == 0) raise_status(ctx.status, PKV_STATUS_BAD_PAGE);
                     const int st = seq % NS;
                     if (!warp_wait(&empty[st], ((seq / NS) & 1) ^ 1, ctx)) {
                         stop = true;
                         break;
                     }
                     if (lane == 0) {
-                        if (nvalid > 0)
-                            mbar_arrive_expect_tx(&full[st], nvalid * 2 * kRowBytes);
-                        else
+                        if (ok) {
+                            uint8_t* dst = smem + L::off_stage + st * kStageBytes;
+                            const int z = phys * kPageSize;
+                            mbar_arrive_expect_tx(&full[st], kStageBytes);
+                            tma_load_3d(dst, &p.tmap_k, 0, sl.h, z, &full[st], pol);
+                            tma_load_3d(dst + kBoxBytes, &p.tmap_k, 64, sl.h, z, &full[st], pol);
+                            tma_load_3d(dst + 2 * kBoxBytes, &p.tmap_v, 0, sl.h, z, &full[st], pol);
+                            tma_load_3d(dst + 3 * kBoxBytes, &p.tmap_v, 64, sl.h, z, &full[st], pol);
+                        } else {
                             mbar_arrive(&full[st]);
+                        }
                     }
                     __syncwarp();
-                    if (row < nvalid) {
-                        const char* src =
-                            pool + ((((size_t)phys * kPageSize + row) * Hkv + sl.h) * (size_t)kRowBytes);
-                        bulk_g2s_hint(smem + L::off_stage + st * kStageBytes + dst_off, src, kRowBytes, &full[st],
-                                      pol);
-                    }
                     ++seq;
                 }
                 if (stop) break;
@@ -264,9 +275,10 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 2) decode_kernel(const DecodeP
         const int g0 = lane >> 2;        // query head (row of the mma tile) this lane holds
         const int tq = 2 * (lane & 3);   // first token column this lane holds in each 8-token half
         const int mi = lane >> 3, mr = lane & 7;
-        // per-lane ldmatrix row offsets inside a stage (bytes)
-        const uint32_t k_lane = ((mi >> 1) * 8 + mr) * kSmemRow + (mi & 1) * 16;
-        const uint32_t v_lane = kPageSize * kSmemRow + ((mi & 1) * 8 + mr) * kSmemRow + (mi >> 1) * 16;
+        // ldmatrix row addresses: K (non-transposed) rows = tokens (mi >> 1) * 8 + mr, chunk parity mi & 1;
+        // V (transposed) rows = tokens (mi & 1) * 8 + mr, chunk parity mi >> 1.
+        const int k_row = ((mi >> 1) << 3) + mr, k_par = mi & 1;
+        const int v_row = ((mi & 1) << 3) + mr, v_par = mi >> 1;
         const uint32_t stage0 = smem_addr(smem + L::off_stage);
         float* comb_o = reinterpret_cast<float*>(smem + L::off_comb);
         float2* comb_ml = reinterpret_cast<float2*>(smem + L::off_comb_ml);
@@ -281,14 +293,16 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 2) decode_kernel(const DecodeP
             uint32_t qa[8][4];
             {
                 const uint8_t* qs = smem + L::off_q + ts * L::kQRowsBytes;
+                const bool lo = g0 < G && sl.npages > 0;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const int col = (ks * 16 + tq) * 2;
-                    qa[ks][0] = (g0 < G && sl.npages > 0) ? *reinterpret_cast<const uint32_t*>(qs + g0 * kSmemRow + col) : 0u;
-                    qa[ks][2] = (g0 < G && sl.npages > 0) ? *reinterpret_cast<const uint32_t*>(qs + g0 * kSmemRow + col + 16) : 0u;
+                    qa[ks][0] = lo ? *reinterpret_cast<const uint32_t*>(qs + g0 * kRowBytes + col) : 0u;
+                    qa[ks][2] = lo ? *reinterpret_cast<const uint32_t*>(qs + g0 * kRowBytes + col + 16) : 0u;
                     if constexpr (G > 8) {
-                        qa[ks][1] = (g0 + 8 < G && sl.npages > 0) ? *reinterpret_cast<const uint32_t*>(qs + (g0 + 8) * kSmemRow + col) : 0u;
-                        qa[ks][3] = (g0 + 8 < G && sl.npages > 0) ? *reinterpret_cast<const uint32_t*>(qs + (g0 + 8) * kSmemRow + col + 16) : 0u;
+                        const bool hi = g0 + 8 < G && sl.npages > 0;
+                        qa[ks][1] = hi ? *reinterpret_cast<const uint32_t*>(qs + (g0 + 8) * kRowBytes + col) : 0u;
+                        qa[ks][3] = hi ? *reinterpret_cast<const uint32_t*>(qs + (g0 + 8) * kRowBytes + col + 16) : 0u;
                     } else {
                         qa[ks][1] = 0u;
                         qa[ks][3] = 0u;
@@ -313,12 +327,25 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 2) decode_kernel(const DecodeP
                 }
                 const int nvalid = min(kPageSize, sl.seq_len - (sl.page_begin + i) * kPageSize);
                 const uint32_t sbase = stage0 + st * kStageBytes;
-                // S = Q K^T: two n8 tiles (tokens 0-7 and 8-15), k = head_dim in 8 steps
+                if (nvalid < kPageSize) {
+                    // The boxes always carry 16 token rows; rows past the row's length hold whatever the pool has
+                    // there. Their scores are masked below; their V rows are zeroed so 0 * (non-finite) cannot
+                    // reach the accumulator.
+                    uint8_t* vbase = smem + L::off_stage + st * kStageBytes + 2 * kBoxBytes;
+                    for (int e = lane; e < 2 * kPageSize * 8; e += 32) {
+                        const int box = e >> 7, r = (e >> 3) & 15, c = e & 7;
+                        if (r >= nvalid)
+                            *reinterpret_cast<int4*>(vbase + box * kBoxBytes + r * 128 + c * 16) = make_int4(0, 0, 0, 0);
+                    }
+                    __syncwarp();
+                }
+                // S = Q K^T: two n8 tiles (tokens 0-7 and 8-15), k = head_dim in 8 steps of 16 columns
                 float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4(sbase + k_lane + ks * 32, b0, b1, b2, b3);
+                    const uint32_t box = sbase + (ks >> 2) * kBoxBytes;
+                    ldsm_x4(box + swz(k_row, ((ks & 3) << 1) | k_par), b0, b1, b2, b3);
                     mma_16816(s0, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
                     mma_16816(s1, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
                 }
@@ -339,8 +366,8 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 2) decode_kernel(const DecodeP
                 for (int e = 0; e < 4; ++e) pr[e] = fast_exp2(x[e] - mu);
                 l_lo = l_lo * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
                 m_lo = mn;
-                uint32_t pa0 = pack_half2(pr[0], pr[1]);
-                uint32_t pa2 = pack_half2(pr[2], pr[3]);
+                const uint32_t pa0 = pack_half2(pr[0], pr[1]);
+                const uint32_t pa2 = pack_half2(pr[2], pr[3]);
                 uint32_t pa1 = 0u, pa3 = 0u;
                 float alpha_hi = 1.f;
                 if constexpr (G > 8) {
@@ -376,10 +403,12 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 2) decode_kernel(const DecodeP
 #pragma unroll
                 for (int n2 = 0; n2 < 8; ++n2) {
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4_trans(sbase + v_lane + n2 * 32, b0, b1, b2, b3);
+                    const uint32_t box = sbase + (2 + (n2 >> 2)) * kBoxBytes;
+                    ldsm_x4_trans(box + swz(v_row, ((n2 & 3) << 1) | v_par), b0, b1, b2, b3);
                     mma_16816(o[2 * n2], pa0, pa1, pa2, pa3, b0, b1);
                     mma_16816(o[2 * n2 + 1], pa0, pa1, pa2, pa3, b2, b3);
                 }
+                if (nvalid < kPageSize) fence_proxy_async_smem();  // zero stores before the next TMA write
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[st]);
             }

@@ -4,6 +4,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
+
 #include "pkv.h"
 
 namespace pkv {
@@ -15,8 +17,12 @@ constexpr int kTokenHeadBytes = 2 * kRowBytes;        // K + V of one token for 
 constexpr int kStateBytes = (kHeadDim + 2) * 4;       // (m, l, acc[d]) in fp32
 constexpr int kWsAlign = 256;
 
-// Arguments of the decode kernel (passed by value as a kernel parameter).
+// Arguments of the decode kernel (passed by value as a __grid_constant__ kernel parameter).
 struct DecodeParams {
+    // TMA descriptors of the K and V pools viewed as 3-D tensors (d, Hkv, num_pages * page_size), box
+    // (64, 1, page_size), 128-byte swizzle: one box is half of one KV head's rows of one page.
+    CUtensorMap tmap_k;
+    CUtensorMap tmap_v;
     const void* q;
     const void* k_pool;
     const void* v_pool;
