@@ -6,8 +6,9 @@ page size 16, fp16 ~N(0,1), start length from {4096, 8192, 16384, 32768}, 64 ste
 shuffled in a 2^16-page pool) over the held-out seeds 5-9, cycled until K steps have run.
 
 Timing: every step is bracketed by CUDA events on the launching stream; the decode kernel alone by a second pair.
-Between steps an L2 flush (a 256 MiB write, larger than the 129 MB L2) runs outside the step's events, so every
-step reads its KV from HBM, as it would after the other layers of a model ran. `value` = tokens / sum of step
+Between steps an L2 flush runs outside the step's events: a 256 MiB write (larger than the 129 MB L2), then a
+256 MiB read of another buffer, so every step reads its KV from HBM, as it would after the other layers of a model
+ran, and starts with an L2 that holds no dirty lines (the write-back of the flush buffer is not charged to the step). `value` = tokens / sum of step
 times. `e2e` repeats the steps through the same C ABI from pinned host buffers: per step the host->device copies of
 q, seq_lens, the block table and the new token's K/V, the step, and the device->host copy of out, all inside the
 events. `cpu_baseline` times the fp64 oracle on the host on a bounded sample of the same trace steps.
@@ -146,6 +147,19 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+class L2Flush:
+    """Evicts the L2 between steps: a write of one buffer larger than L2, then a read of another, which leaves
+    only clean lines behind."""
+
+    def __init__(self, torch, dev):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.sink = self.r.sum()
+
+
 # ------------------------------------------------------------------------------------------------ workload
 def build_workload(config: str, seeds, dev, pool_pages: int = 0):
     """Device tensors for every step of every trace: pools with all pages a trace will use, per-step q, block
@@ -176,6 +190,14 @@ def build_workload(config: str, seeds, dev, pool_pages: int = 0):
                           "q": torch.from_numpy(q).to(dev), "bt": torch.from_numpy(bt).to(dev),
                           "lens": torch.from_numpy(lens).to(dev), "new_phys": new_phys, "new_slot": new_slot})
     return traces, steps
+
+
+def decode_fit(kv_bytes, dec_ms):
+    """Least-squares fit of decode time = fixed + bytes / bandwidth over the timed steps."""
+    if len(set(np.round(kv_bytes / 1e6, 3))) < 2:
+        return None
+    slope, icpt = np.polyfit(kv_bytes, dec_ms * 1e3, 1)
+    return {"fixed_us": float(icpt), "incremental_gbs": float(1e-3 / slope) if slope > 0 else None}
 
 
 def make_plan(pkv, problem, lens, sms, args):
@@ -294,7 +316,7 @@ def run_ours(args):
     plan_us = 1e6 * (time.perf_counter() - t0) / len(steps)
     ws = pkv.alloc_workspace(max(p.ws_bytes for p in plans), dev)
     out = torch.empty((B, Hq, d), dtype=torch.float16, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
 
     def launch(k):
@@ -304,7 +326,7 @@ def run_ours(args):
                             scale, ws, out, stream)
 
     for k in range(args.warmup):
-        flush.zero_()
+        flush()
         launch(k)
     torch.cuda.synchronize()
     if pkv.pkv_read_status(ws) != 0:
@@ -326,7 +348,7 @@ def run_ours(args):
         s = steps[j]
         tr, kpool, vpool = traces[s["trace"]]
         plan, problem = plans[j], problems[s["trace"]]
-        flush.zero_()
+        flush()
         e = ev[k]
         e[0].record(stream)
         if plan.variant == pkv.PKV_VARIANT_WORKQUEUE:
@@ -344,6 +366,8 @@ def run_ours(args):
     clocks.mark_stop()
     step_ms = np.array([e[0].elapsed_time(e[3]) for e in ev])
     dec_ms = np.array([e[1].elapsed_time(e[2]) for e in ev])
+    build_ms = np.array([e[0].elapsed_time(e[1]) for e in ev])
+    merge_ms = np.array([e[2].elapsed_time(e[3]) for e in ev])
     kv_bytes = np.array([plans[(args.warmup + k) % len(steps)].kv_bytes for k in range(K)])
     tokens = K * B
     total_ms = float(step_ms.sum())
@@ -359,7 +383,7 @@ def run_ours(args):
         j = k % len(steps)
         s = steps[j]
         tr, kpool, vpool = traces[s["trace"]]
-        flush.zero_()
+        flush()
         torch.cuda.synchronize()
         w0 = time.perf_counter()
         plan = make_plan(pkv, problems[s["trace"]], s["lens_host"], sms, args)
@@ -398,13 +422,15 @@ def run_ours(args):
         "impl": "ours",
         "config": {"workload": args.config, "seeds": seeds, "batch": B, "num_q_heads": Hq, "num_kv_heads": Hkv,
                    "head_dim": d, "page_size": tr0.ps, "pool_pages": tr0.num_pages, "trace_steps": len(steps),
-                   "l2": "flushed between steps (256 MiB write outside the step events)",
+                   "l2": "flushed between steps outside the step events (256 MiB write, then 256 MiB read)",
                    "variant": args.variant, "variants_used": variants,
                    "splits_min_max": [int(min(splits)), int(max(splits))], "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "kernel": "pkv decode_kernel", "peak_source": f"hbm_gbs ({peak_kind})",
                      "algorithmic_bytes_per_step": float(kv_bytes.mean())},
         "decode_us_mean": 1e3 * float(dec_ms.mean()), "step_us_mean": 1e3 * float(step_ms.mean()),
+        "build_us_mean": 1e3 * float(build_ms.mean()), "merge_us_mean": 1e3 * float(merge_ms.mean()),
+        "decode_fit": decode_fit(kv_bytes, dec_ms),
         "step_us_p50": 1e3 * float(np.median(step_ms)), "kv_gbs_step": float(kv_bytes.sum() / (step_ms.sum() * 1e-3)) / 1e9,
         "wall_us_per_step": wall_us, "wall_tokens_per_s": B / (wall_us * 1e-6), "plan_us": plan_us,
         "timed_wall_s": wall_timed, "gpu_launches": launches, "device_status": status,
@@ -439,7 +465,7 @@ def run_e2e(args, pkv, torch, traces, steps, plans, problems, ws, flush, stream,
         s, hs = steps[k], host[k]
         tr, kpool, vpool = traces[s["trace"]]
         plan = plans[k]
-        flush.zero_()
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         q_d.copy_(hs["q"], non_blocking=True)

@@ -13,7 +13,7 @@
 //               one elected lane issues four 3-D TMA tensor copies (K and V of KV head h, each as two 64-column
 //               boxes of the page's 16 token rows, 128-byte swizzled) into a ring stage; completion is counted in
 //               bytes on the stage's mbarrier;
-//   warps 0..NCW-1 consumers: page i of a task goes to warp i % NCW. Per page: S = Q K^T on mma.sync m16n8k16
+//   warps 0..NCW-1 consumers: page j of the CTA's page sequence goes to warp j % NCW. Per page: S = Q K^T on mma.sync m16n8k16
 //               (rows = the G query heads, columns = the 16 tokens), masking of slots past the row length, online
 //               softmax in base 2 in registers with quad shuffles, O += P V on mma.sync. At the end of the task the
 //               NCW warps combine their states through shared memory and write either the normalised fp16 output
@@ -106,6 +106,7 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 
 template <int G, int NCW, int NS, int NTS>
 __global__ void __launch_bounds__((NCW + 2) * 32, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
+    static_assert(NS % NCW == 0, "each ring stage must map to one consumer warp");
     using L = Layout<G, NCW, NS, NTS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
@@ -318,7 +319,10 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 2) decode_kernel(const __grid_
             float m_lo = -INFINITY, l_lo = 0.f, m_hi = -INFINITY, l_hi = 0.f;
             bool aborted = false;
 
-            for (int i = w; i < sl.npages; i += NCW) {
+            // Page j of the CTA's page sequence lives in stage j % NS and is consumed by warp j % NCW. With
+            // NS % NCW == 0 a stage is always consumed by the same warp, which has therefore finished the stage's
+            // previous page before it waits on the stage again: the parity wait can never match a phase two back.
+            for (int i = (w - seq % NCW + NCW) % NCW; i < sl.npages; i += NCW) {
                 const int j = seq + i;
                 const int st = j % NS;
                 if (!warp_wait(&full[st], (j / NS) & 1, ctx)) {
@@ -483,9 +487,15 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 2) decode_kernel(const __grid_
     }
 }
 
-constexpr int kNCW = 4;
-constexpr int kNS = 8;
-constexpr int kNTS = 4;
+#ifndef PKV_DECODE_CONSUMERS
+#define PKV_DECODE_CONSUMERS 4
+#endif
+#ifndef PKV_DECODE_STAGES
+#define PKV_DECODE_STAGES 8
+#endif
+constexpr int kNCW = PKV_DECODE_CONSUMERS;  // consumer warps per CTA
+constexpr int kNS = PKV_DECODE_STAGES;      // pages in flight per CTA
+constexpr int kNTS = 4;                     // task slots (scheduler look-ahead)
 
 template <int G>
 int launch_g(const DecodeParams& p, int grid, cudaStream_t stream) {

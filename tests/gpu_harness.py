@@ -43,10 +43,11 @@ class Step:
         self.sms = torch.cuda.get_device_properties(self.q.device).multi_processor_count
         self._ref = None
 
-    def plan(self, variant=None, chunk=1):
+    def plan(self, variant=None, chunk=1, sms=None):
+        sms = self.sms if sms is None else sms
         if variant is None:
-            return pkv.pkv_plan(self.problem, self.lens_host, self.sms)
-        return pkv.pkv_plan_fixed(self.problem, self.lens_host, self.sms, variant, chunk)
+            return pkv.pkv_plan(self.problem, self.lens_host, sms)
+        return pkv.pkv_plan_fixed(self.problem, self.lens_host, sms, variant, chunk)
 
     def run(self, plan, ws=None):
         if ws is None:

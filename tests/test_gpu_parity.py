@@ -126,6 +126,19 @@ def test_traces_policy_and_forced_schedules(name, seed, steps):
             assert_close(out, ref, f"{name} seed {seed} step {t} {plan.describe()}")
 
 
+@pytest.mark.parametrize("sms", [1, 3])
+def test_few_ctas_many_task_boundaries(sms):
+    """A grid of 2 or 6 CTAs runs hundreds of tasks each, with page counts per task that are not multiples of the
+    consumer-warp count, so the shared-memory page ring wraps across many task boundaries."""
+    tr = make_trace("b8_zipf", 5, steps=1)
+    step = Step(tr, 0)
+    ref = step.reference()
+    for variant, chunk in ((SPLIT, 5), (WQ, 3), (WQ, 7), (SPLIT, 1), (SINGLE, 1)):
+        out, _, status = step.run(step.plan(variant, chunk, sms=sms))
+        assert status == 0
+        assert_close(out, ref, f"grid of {2 * sms} CTAs, variant {variant}, c={chunk}")
+
+
 def test_stress_sampled_pairs():
     tr = make_trace("stress", 5, steps=1)
     step = Step(tr, 0)
