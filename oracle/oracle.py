@@ -7,8 +7,9 @@ abstract: the exact-length-bucket schedule launches once per distinct length, th
 split kernel and a merge kernel.
 
 Parity status: ``launch_counts`` is pinned by the pages' printed 16.00 / 2.00 launches per step on bimodal B8
-(tests/golden/launch_fanout_b8_bimodal.txt). ``merge_state_bytes`` is *parity unpinned*: the pages print a
-~37 % reduction but not the split size it was measured at.
+(tests/golden/launch_fanout_b8_bimodal.txt). ``merge_state_bytes`` is pinned by byte counts derived by hand for
+small cases (tests/test_golden_counters.py); the pages' ~37 % reduction cannot pin it, because the pages do not
+state the split size it was measured at.
 """
 
 from __future__ import annotations
@@ -191,7 +192,7 @@ def merge_state_bytes(seq_lens, page_size: int, num_q_heads: int, num_kv_heads: 
     """Bytes of partial states written then read by the merge, rectangular split grid vs compact workqueue.
 
     A state is (m, l, acc[head_dim]) in fp32. The rectangular grid holds B*Hq*max_b(S_b) states (empty splits
-    write neutral states); the workqueue holds sum_b Hq*S_b. Parity unpinned (see the module docstring).
+    write neutral states); the workqueue holds sum_b Hq*S_b. Every state is written once and read once.
     """
     L = np.asarray(seq_lens, dtype=np.int64)
     P = (L + page_size - 1) // page_size

@@ -41,3 +41,26 @@ def test_merge_state_traffic_workqueue_never_exceeds_rect():
         for c in (8, 16, 32, 64):
             mb = oracle.merge_state_bytes(tr.seq_lens(0), 16, 32, 8, c)
             assert mb["workqueue"] <= mb["rect"]
+
+
+def test_merge_state_bytes_hand_derived():
+    """Byte counts worked out by hand for small cases.
+
+    One partial state is (m, l, acc[d]) in fp32: 4 * (d + 2) bytes, 520 B at d = 128 and 24 B at d = 4. Every
+    state is written once by the decode kernel and read once by the merge, so traffic = 2 * states * state bytes.
+    Row b has P_b = ceil(L_b / 16) pages and S_b = ceil(P_b / c) splits; the rectangular grid holds
+    B * Hq * max_b S_b states, the workqueue sum_b Hq * S_b.
+    """
+    # L = [16, 200]: P = [1, 13]. c = 1: S = [1, 13] -> rect 2*32*13 states, workqueue 32*14 states.
+    mb = oracle.merge_state_bytes([16, 200], 16, 32, 8, 1)
+    assert mb == {"rect": 2 * (2 * 32 * 13) * 520, "workqueue": 2 * (32 * 14) * 520}
+    # c = 4: S = [1, 4] -> rect 2*32*4 states, workqueue 32*5 states.
+    mb = oracle.merge_state_bytes([16, 200], 16, 32, 8, 4)
+    assert mb == {"rect": 2 * (2 * 32 * 4) * 520, "workqueue": 2 * (32 * 5) * 520}
+    # an empty row has no states in the workqueue but still a full row of neutral states in the rectangular grid:
+    # L = [0, 17]: P = [0, 2], c = 1: S = [0, 2] -> rect 2*8*2 states (Hq = 8), workqueue 8*2; d = 4 -> 24 B each
+    mb = oracle.merge_state_bytes([0, 17], 16, 8, 2, 1, head_dim=4)
+    assert mb == {"rect": 2 * (2 * 8 * 2) * 24, "workqueue": 2 * (8 * 2) * 24}
+    # a page count that is not a multiple of c rounds up: L = [33] is 3 pages, c = 2 gives 2 splits
+    mb = oracle.merge_state_bytes([33], 16, 4, 4, 2)
+    assert mb == {"rect": 2 * (1 * 4 * 2) * 520, "workqueue": 2 * (4 * 2) * 520}
