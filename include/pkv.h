@@ -198,6 +198,31 @@ int pkv_read_status(void* ws, size_t ws_bytes, void* stream, uint32_t* status);
 /* Number of kernel launches pkv_decode_step enqueues for this plan. */
 int pkv_plan_launches(const pkv_plan_t* plan);
 
+/* Size of the library-owned workspace behind pkv_decode_step_static (16 MiB per GPU). */
+#define PKV_STATIC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * pkv_decode_step for callers that cannot allocate device memory. The paper has no counterpart: it is a
+ * convenience of this library. Some callers cannot call cudaMalloc where they run a decode step (a plug-in whose
+ * host application owns every allocation, code running inside another framework's memory pool, a serving loop
+ * that must not allocate after start-up), so this call takes the same inputs and output as pkv_decode_step but
+ * keeps the workspace in a fixed array of PKV_STATIC_SCRATCH_BYTES in the library's own device memory. Every GPU
+ * that loads libpkv.so holds that array until the process exits. The call itself allocates nothing.
+ *   plan, problem, q, k_pool, v_pool, block_table, seq_lens_dev, scale, out, stream: as for pkv_decode_step
+ *     (out is always required).
+ *   status_dev: NULL, or a 4-byte aligned device uint32_t that receives this step's PKV_STATUS_* bits (stream
+ *     ordered, after the step).
+ * Errors: PKV_E_WS_TOO_SMALL if plan->ws_bytes exceeds PKV_STATIC_SCRATCH_BYTES (choose a plan with fewer tasks,
+ * e.g. a larger chunk_pages); otherwise the errors of pkv_decode_step. Nothing is enqueued on error.
+ * The first call on a device looks up the array's device address (once per device, with that device current);
+ * make that first call before any stream capture. All calls share the one array and it keeps the last call's
+ * contents; the call clears the status word after each step. Calls whose work overlaps on the GPU (other streams,
+ * or other host threads on the same device) race on the array: order them on one stream.
+ */
+int pkv_decode_step_static(const pkv_plan_t* plan, const pkv_problem* problem, const void* q, const void* k_pool,
+                           const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev, float scale,
+                           void* out, uint32_t* status_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
