@@ -26,8 +26,10 @@
  * Supported: head_dim = 128, page_size = 16, G = Hq / Hkv in {1, 2, 4, 8, 16}, B <= PKV_MAX_BATCH.
  *
  * Ownership: the caller owns every buffer, including the workspace (sized by pkv_plan_t.ws_bytes, 256-byte
- * aligned, prepared once with pkv_workspace_init). The library allocates no memory and keeps no per-call state;
- * the only process-wide state is a once-per-device kernel attribute set-up.
+ * aligned, zeroed once with pkv_workspace_init). The library allocates no memory and keeps no per-call state;
+ * the only process-wide state is a once-per-device kernel attribute set-up and a cache of TMA descriptors keyed by
+ * pool address. Between steps the workspace's counters are back at zero; after a step that raised
+ * PKV_STATUS_TIMEOUT or PKV_STATUS_TASKS, call pkv_workspace_init again before the next step.
  * Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). Every device call only
  * enqueues work and returns; pkv_plan is host-only and synchronous.
  * Errors: every call returns PKV_OK (0) or a negative PKV_E_* code and enqueues nothing on error. Errors the
@@ -44,7 +46,7 @@
 extern "C" {
 #endif
 
-#define PKV_VERSION 1
+#define PKV_VERSION 2
 
 #define PKV_OK 0
 #define PKV_E_INVAL (-1)        /* bad shape, negative size, inconsistent plan/problem */
@@ -99,15 +101,19 @@ typedef struct pkv_plan_t {
     int32_t chunk_pages; /* c: pages per split; row b has S_b = ceil(ceil(L_b / page_size) / c) splits */
     int32_t num_splits;  /* S = max_b S_b (extent of the rectangular grid) */
     int32_t num_tasks;   /* tasks the decode kernel runs (single: B*Hkv; split: B*Hkv*S; wq: sum_b Hkv*S_b) */
-    int32_t grid_ctas;   /* persistent decode grid size */
+    int32_t grid_ctas;   /* persistent decode grid size (resident CTAs, at most one wave) */
     int32_t group;       /* G = Hq / Hkv */
     int32_t num_sms;     /* SM count the plan was made for */
-    int32_t reserved;
+    int32_t fuse_merge;  /* split / workqueue: 1 = pkv_decode merges the split states itself (the last task of every
+                            (row, KV head) to finish merges them and writes out; pkv_merge is then a no-op);
+                            0 = pkv_decode writes partial states only and pkv_merge combines them. The planners set
+                            1; a caller may set 0 (the workspace layout does not depend on it). */
     pkv_problem problem; /* copy of the problem the plan was made for; later calls must pass an equal one */
     int64_t task_capacity;  /* task slots reserved in the workspace */
     int64_t state_capacity; /* partial-state slots reserved in the workspace */
     int64_t ws_bytes;       /* workspace bytes this plan needs */
-    int64_t off_row_off;    /* byte offsets inside the workspace: int32 row_off[B] */
+    int64_t off_counters;   /* byte offsets inside the workspace: uint32 arrivals[B][Hkv] (fused merge) */
+    int64_t off_row_off;    /*   int32 row_off[B] */
     int64_t off_row_splits; /*   int32 row_splits[B] */
     int64_t off_tasks;      /*   int4 tasks[task_capacity] */
     int64_t off_ml;         /*   float2 (m, l) per state */
@@ -127,10 +133,11 @@ typedef struct pkv_task {
 
 /* Workspace header at offset 0 (256 bytes). */
 typedef struct pkv_ws_header {
-    uint32_t queue_head;  /* next task to claim (workqueue) */
+    uint32_t queue_head;  /* next task to claim (workqueue); re-armed to 0 by the builder and after every decode */
     int32_t task_count;   /* tasks written by the last pkv_build_worklist */
     uint32_t status;      /* PKV_STATUS_* bits, sticky until pkv_read_status clears them */
-    uint32_t reserved[61];
+    uint32_t ctas_done;   /* decode CTAs that finished claiming (workqueue); back to 0 after every decode */
+    uint32_t reserved[60];
 } pkv_ws_header;
 
 /* Library version (PKV_VERSION). */
@@ -142,7 +149,7 @@ const char* pkv_strerror(int code);
 /* Validates a problem against the supported set. Host only. */
 int pkv_check_problem(const pkv_problem* problem);
 
-/* Fills *policy with the built-in cost-model constants (fitted on the calibration traces, seeds 0-4). */
+/* Fills *policy with the built-in cost-model constants. */
 void pkv_policy_default(pkv_policy* policy);
 
 /*
@@ -159,21 +166,35 @@ int pkv_plan(const pkv_problem* problem, const int32_t* seq_lens_host, int32_t n
 int pkv_plan_fixed(const pkv_problem* problem, const int32_t* seq_lens_host, int32_t num_sms, int32_t variant,
                    int32_t chunk_pages, int32_t ctas_per_sm, pkv_plan_t* plan);
 
-/* Zeroes the workspace header (queue head, task count, status) on `stream`. Call once after allocating. */
+/* Zeroes the whole workspace (header, arrival counters) on `stream`. Call once after allocating, and again after
+ * a step that raised PKV_STATUS_TIMEOUT or PKV_STATUS_TASKS. */
 int pkv_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /*
- * Worklist builder (compact workqueue, "Compact Workqueue"): from device seq_lens computes S_b, an exclusive
- * prefix sum of Hkv*S_b, and writes the non-empty tasks in (b, h_kv, s) order, row_off/row_splits, the task count
- * and resets the queue head. Only for plans with variant PKV_VARIANT_WORKQUEUE (returns PKV_E_INVAL otherwise).
+ * Worklist builder (gist.science technical summary, "Methodologie" 1, "Compact Workqueue": a 1-D grid of tasks for
+ * the non-empty row / KV-head / split intervals only). From device seq_lens computes S_b, an exclusive prefix sum of
+ * Hkv*S_b, and writes the non-empty tasks in (b, h_kv, s) order, row_off/row_splits, the task count and resets the
+ * queue head. Only for plans with variant PKV_VARIANT_WORKQUEUE (returns PKV_E_INVAL otherwise). The decode that
+ * follows it on the same stream may start its prologue while the builder runs (programmatic dependent launch); it
+ * reads nothing the builder writes before the builder has finished.
  */
 int pkv_build_worklist(const pkv_plan_t* plan, const pkv_problem* problem, const int32_t* seq_lens_dev, void* ws,
                        size_t ws_bytes, void* stream);
 
 /*
- * Decode kernel. single: writes out. split / workqueue: writes the partial (m, l, acc) state of every task's G
- * query heads into the workspace (empty rectangular splits write m = -inf, l = 0, acc = 0); follow with
- * pkv_merge. scale multiplies q.k (use 1/sqrt(head_dim)). out may be NULL unless the variant is single.
+ * Decode kernel: grouped-query attention of every row over its pages, read in place through block_table (gist.science
+ * technical summary, "Methodologie" 1: "Layout" -- no repacking into contiguous tensors; "Sequentie Splitting" --
+ * each split computes a partial online-softmax state; "Row-Local Bounds" -- split ranges from each row's true length,
+ * empty splits write a neutral state; v1/v2 abstracts: work mapped by KV-head group). For query head hq of row b
+ * (KV head hkv = hq / G) it computes softmax(scale * q.K^T) V over the row's seq_lens[b] tokens.
+ *   single: one task per (row, KV head); writes the normalised output to out.
+ *   split / workqueue: one task per (row, KV head, split) writes the partial (m, l, acc) state of its G query heads
+ *     into the workspace (empty rectangular splits write m = -inf, l = 0, acc = 0). With plan->fuse_merge = 1 the
+ *     last task of each (row, KV head) also merges that pair's states and writes out; with 0, follow with pkv_merge.
+ *   workqueue: runs the list the last pkv_build_worklist wrote into ws (call it first, on the same stream).
+ * scale multiplies q.k (use 1/sqrt(head_dim)). out may be NULL only for split / workqueue plans with fuse_merge 0.
+ * Rows longer than the plan's lengths (seq_lens grew after pkv_plan) raise PKV_STATUS_TASKS; their extra pages are
+ * not read.
  */
 int pkv_decode(const pkv_plan_t* plan, const pkv_problem* problem, const void* q, const void* k_pool,
                const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev, float scale, void* ws,
@@ -182,7 +203,8 @@ int pkv_decode(const pkv_plan_t* plan, const pkv_problem* problem, const void* q
 /*
  * Log-sum-exp merge ("Sequentie Splitting": a separate merge combines the split states exactly):
  * out[b,hq] = sum_s e^(m_s - M) acc_s / sum_s e^(m_s - M) l_s with M = max_s m_s over non-neutral states; a row
- * with no non-empty state gets 0. For split and workqueue plans; a single plan returns PKV_OK without work.
+ * with no non-empty state gets 0. For split and workqueue plans with fuse_merge = 0; for single plans and fused
+ * plans it returns PKV_OK without work.
  */
 int pkv_merge(const pkv_plan_t* plan, const pkv_problem* problem, void* ws, size_t ws_bytes, void* out,
               void* stream);

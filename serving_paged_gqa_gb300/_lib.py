@@ -58,16 +58,17 @@ class Policy(ctypes.Structure):
 class Plan(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int32), ("chunk_pages", ctypes.c_int32), ("num_splits", ctypes.c_int32),
                 ("num_tasks", ctypes.c_int32), ("grid_ctas", ctypes.c_int32), ("group", ctypes.c_int32),
-                ("num_sms", ctypes.c_int32), ("reserved", ctypes.c_int32), ("problem", Problem),
+                ("num_sms", ctypes.c_int32), ("fuse_merge", ctypes.c_int32), ("problem", Problem),
                 ("task_capacity", ctypes.c_int64), ("state_capacity", ctypes.c_int64),
-                ("ws_bytes", ctypes.c_int64), ("off_row_off", ctypes.c_int64), ("off_row_splits", ctypes.c_int64),
+                ("ws_bytes", ctypes.c_int64), ("off_counters", ctypes.c_int64), ("off_row_off", ctypes.c_int64),
+                ("off_row_splits", ctypes.c_int64),
                 ("off_tasks", ctypes.c_int64), ("off_ml", ctypes.c_int64), ("off_acc", ctypes.c_int64),
                 ("predicted_us", ctypes.c_double), ("kv_bytes", ctypes.c_double)]
 
     def describe(self) -> dict:
         return {"variant": VARIANT_NAMES.get(self.variant, self.variant), "chunk_pages": self.chunk_pages,
                 "num_splits": self.num_splits, "num_tasks": self.num_tasks, "grid_ctas": self.grid_ctas,
-                "ws_bytes": self.ws_bytes, "predicted_us": self.predicted_us}
+                "fuse_merge": self.fuse_merge, "ws_bytes": self.ws_bytes, "predicted_us": self.predicted_us}
 
 
 _lib = None

@@ -23,7 +23,10 @@ int check_plan(const pkv_plan_t* plan, const pkv_problem* pr, const void* ws, si
     if (!same_problem(plan->problem, *pr)) return PKV_E_INVAL;
     if (plan->variant < PKV_VARIANT_SINGLE || plan->variant > PKV_VARIANT_WORKQUEUE) return PKV_E_INVAL;
     if (plan->group != pr->num_q_heads / pr->num_kv_heads || plan->grid_ctas <= 0 || plan->chunk_pages <= 0 ||
-        plan->num_splits <= 0 || plan->num_tasks < 0)
+        plan->num_splits <= 0 || plan->num_tasks < 0 || (plan->fuse_merge != 0 && plan->fuse_merge != 1))
+        return PKV_E_INVAL;
+    if (plan->off_counters < (int64_t)sizeof(pkv_ws_header) ||
+        plan->off_counters + 4 * (int64_t)pr->batch * pr->num_kv_heads > plan->ws_bytes)
         return PKV_E_INVAL;
     if (!aligned(ws, kWsAlign)) return PKV_E_ALIGN;
     if ((int64_t)ws_bytes < plan->ws_bytes) return PKV_E_WS_TOO_SMALL;
@@ -115,7 +118,7 @@ extern "C" int pkv_workspace_init(void* ws, size_t ws_bytes, void* stream) {
     if (!ws) return PKV_E_NULLPTR;
     if (ws_bytes < sizeof(pkv_ws_header)) return PKV_E_WS_TOO_SMALL;
     if (!aligned(ws, kWsAlign)) return PKV_E_ALIGN;
-    return cuda_rc(cudaMemsetAsync(ws, 0, sizeof(pkv_ws_header), static_cast<cudaStream_t>(stream)));
+    return cuda_rc(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
 }
 
 extern "C" int pkv_build_worklist(const pkv_plan_t* plan, const pkv_problem* pr, const int32_t* seq_lens_dev,
@@ -141,18 +144,53 @@ extern "C" int pkv_build_worklist(const pkv_plan_t* plan, const pkv_problem* pr,
     return cuda_rc(launch_build(p, grid, stream));
 }
 
-extern "C" int pkv_decode(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_pool,
-                          const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev, float scale,
-                          void* ws, size_t ws_bytes, void* out, void* stream) {
+namespace pkv {
+
+int check_decode_args(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_pool,
+                      const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev, float scale,
+                      void* ws, size_t ws_bytes, void* out) {
     int rc = check_plan(plan, pr, ws, ws_bytes);
     if (rc != PKV_OK) return rc;
     if (pr->batch > 0 && (!q || !k_pool || !v_pool || !block_table || !seq_lens_dev)) return PKV_E_NULLPTR;
-    if (plan->variant == PKV_VARIANT_SINGLE && pr->batch > 0 && !out) return PKV_E_NULLPTR;
+    const bool writes_out = plan->variant == PKV_VARIANT_SINGLE || plan->fuse_merge;
+    if (writes_out && pr->batch > 0 && !out) return PKV_E_NULLPTR;
     if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
         !aligned(block_table, 4) || !aligned(seq_lens_dev, 4))
         return PKV_E_ALIGN;
     if (!(scale == scale)) return PKV_E_INVAL;
-    if (plan->num_tasks == 0) return PKV_OK;
+    return PKV_OK;
+}
+
+int decode_step(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_pool,
+                const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev, float scale, void* ws,
+                size_t ws_bytes, void* out, void* stream, bool clear_counters) {
+    int rc = check_decode_args(plan, pr, q, k_pool, v_pool, block_table, seq_lens_dev, scale, ws, ws_bytes, out);
+    if (rc != PKV_OK) return rc;
+    if (clear_counters) {
+        const size_t n = 4 * (size_t)pr->batch * pr->num_kv_heads;
+        if (n > 0 && cudaMemsetAsync(at<char>(ws, plan->off_counters), 0, n, static_cast<cudaStream_t>(stream)) !=
+                         cudaSuccess)
+            return PKV_E_CUDA;
+    }
+    if (plan->variant == PKV_VARIANT_WORKQUEUE) {
+        rc = pkv_build_worklist(plan, pr, seq_lens_dev, ws, ws_bytes, stream);
+        if (rc != PKV_OK) return rc;
+    }
+    rc = pkv_decode(plan, pr, q, k_pool, v_pool, block_table, seq_lens_dev, scale, ws, ws_bytes, out, stream);
+    if (rc != PKV_OK) return rc;
+    return pkv_merge(plan, pr, ws, ws_bytes, out, stream);
+}
+
+}  // namespace pkv
+
+extern "C" int pkv_decode(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_pool,
+                          const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev, float scale,
+                          void* ws, size_t ws_bytes, void* out, void* stream) {
+    int rc = check_decode_args(plan, pr, q, k_pool, v_pool, block_table, seq_lens_dev, scale, ws, ws_bytes, out);
+    if (rc != PKV_OK) return rc;
+    // A workqueue plan may hold no task while its rows still need an output (every row empty); other plans have
+    // tasks whenever B > 0.
+    if (pr->batch == 0) return PKV_OK;
     DecodeParams p{};
     if (pr->num_pages > 0) {
         rc = pool_tensor_map(k_pool, pr->num_pages, pr->num_kv_heads, &p.tmap_k);
@@ -168,6 +206,8 @@ extern "C" int pkv_decode(const pkv_plan_t* plan, const pkv_problem* pr, const v
     p.ml = at<float>(ws, plan->off_ml);
     p.acc = at<float>(ws, plan->off_acc);
     p.tasks = at<const pkv_task>(ws, plan->off_tasks);
+    p.row_splits = at<const int32_t>(ws, plan->off_row_splits);
+    p.counters = at<uint32_t>(ws, plan->off_counters);
     p.hdr = static_cast<pkv_ws_header*>(ws);
     p.B = pr->batch;
     p.Hq = pr->num_q_heads;
@@ -179,15 +219,19 @@ extern "C" int pkv_decode(const pkv_plan_t* plan, const pkv_problem* pr, const v
     p.variant = plan->variant;
     p.num_tasks = plan->num_tasks;
     p.task_capacity = (int32_t)plan->task_capacity;
+    p.fuse_merge = plan->variant != PKV_VARIANT_SINGLE && plan->fuse_merge;
     p.scale_log2 = scale * 1.4426950408889634f;
-    return cuda_rc(launch_decode(p, plan->group, plan->grid_ctas, stream));
+    // The workqueue decode follows its builder: let it start while the builder runs (it reads the builder's output
+    // only after griddepcontrol.wait).
+    const bool pdl = plan->variant == PKV_VARIANT_WORKQUEUE;
+    return cuda_rc(launch_decode(p, plan->group, plan->grid_ctas, pdl, stream));
 }
 
 extern "C" int pkv_merge(const pkv_plan_t* plan, const pkv_problem* pr, void* ws, size_t ws_bytes, void* out,
                          void* stream) {
     int rc = check_plan(plan, pr, ws, ws_bytes);
     if (rc != PKV_OK) return rc;
-    if (plan->variant == PKV_VARIANT_SINGLE) return PKV_OK;
+    if (plan->variant == PKV_VARIANT_SINGLE || plan->fuse_merge) return PKV_OK;
     if (pr->batch > 0 && !out) return PKV_E_NULLPTR;
     if (!aligned(out, 16)) return PKV_E_ALIGN;
     MergeParams p{};
@@ -209,14 +253,8 @@ extern "C" int pkv_merge(const pkv_plan_t* plan, const pkv_problem* pr, void* ws
 extern "C" int pkv_decode_step(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_pool,
                                const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev,
                                float scale, void* ws, size_t ws_bytes, void* out, void* stream) {
-    int rc;
-    if (plan && plan->variant == PKV_VARIANT_WORKQUEUE) {
-        rc = pkv_build_worklist(plan, pr, seq_lens_dev, ws, ws_bytes, stream);
-        if (rc != PKV_OK) return rc;
-    }
-    rc = pkv_decode(plan, pr, q, k_pool, v_pool, block_table, seq_lens_dev, scale, ws, ws_bytes, out, stream);
-    if (rc != PKV_OK) return rc;
-    return pkv_merge(plan, pr, ws, ws_bytes, out, stream);
+    return decode_step(plan, pr, q, k_pool, v_pool, block_table, seq_lens_dev, scale, ws, ws_bytes, out, stream,
+                       false);
 }
 
 extern "C" int pkv_read_status(void* ws, size_t ws_bytes, void* stream, uint32_t* status) {

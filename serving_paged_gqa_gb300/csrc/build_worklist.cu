@@ -17,6 +17,9 @@ constexpr int kThreads = 1024;
 constexpr int kPerThread = PKV_MAX_BATCH / kThreads;
 
 __global__ void __launch_bounds__(kThreads) build_kernel(const BuildParams p) {
+    // The decode launched after this grid waits for its completion before it reads anything written here, so it
+    // may be scheduled at once.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ int32_t s_off[PKV_MAX_BATCH + 1];
     __shared__ int32_t s_pages[PKV_MAX_BATCH];
     __shared__ int32_t s_warp[32];
@@ -82,6 +85,7 @@ __global__ void __launch_bounds__(kThreads) build_kernel(const BuildParams p) {
         if (tid == 0) {
             p.hdr->task_count = count;
             p.hdr->queue_head = 0u;
+            p.hdr->ctas_done = 0u;
             if (total > p.task_capacity) atomicOr(&p.hdr->status, PKV_STATUS_TASKS);
         }
     }

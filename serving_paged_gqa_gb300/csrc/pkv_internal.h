@@ -31,11 +31,14 @@ struct DecodeParams {
     void* out;             // fp16 [B][Hq][d] (single-pass only)
     float* ml;             // float2 (m, l) per state
     float* acc;            // float [state][d]
-    const pkv_task* tasks; // workqueue only
+    const pkv_task* tasks;      // workqueue only
+    const int32_t* row_splits;  // workqueue only: the builder's S_b per row
+    uint32_t* counters;         // fused merge: arrivals per (row, KV head), zero between steps
     pkv_ws_header* hdr;
     int32_t B, Hq, Hkv, num_pages, max_pages;
     int32_t chunk_pages, num_splits, variant, num_tasks, task_capacity;
-    float scale_log2;      // scale * log2(e): scores are kept in base-2 units inside the kernel
+    int32_t fuse_merge;         // 1: the last task of each (row, KV head) merges its states and writes out
+    float scale_log2;           // scale * log2(e): scores are kept in base-2 units inside the kernel
 };
 
 struct BuildParams {
@@ -59,11 +62,30 @@ struct MergeParams {
 };
 
 // Kernel launchers (defined in the .cu files). They return the CUDA error of the launch.
-int launch_decode(const DecodeParams& p, int group, int grid, void* stream);
+int launch_decode(const DecodeParams& p, int group, int grid, bool pdl, void* stream);
 int launch_build(const BuildParams& p, int grid, void* stream);
 int launch_merge(const MergeParams& p, void* stream);
 
+// Validation shared by pkv_decode and the step entry points (PKV_OK or a PKV_E_* code; enqueues nothing).
+int check_decode_args(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_pool,
+                      const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev, float scale,
+                      void* ws, size_t ws_bytes, void* out);
+
+// build (workqueue) + decode + merge on one stream after validating every argument up front; with clear_counters
+// the workspace's arrival counters are zeroed first.
+int decode_step(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_pool, const void* v_pool,
+                const int32_t* block_table, const int32_t* seq_lens_dev, float scale, void* ws, size_t ws_bytes,
+                void* out, void* stream, bool clear_counters);
+
 // Dynamic shared memory of the decode kernel for a group size (0 if unsupported).
 int decode_smem_bytes(int group);
+
+// Resident decode CTAs per SM the kernel is compiled for (its __launch_bounds__ minimum; the register budget of a
+// third CTA does not exist).
+constexpr int kDecodeCtasPerSm = 2;
+
+// Shared memory of one SM usable by resident CTAs (sm_103: 228 KB) and the per-CTA reservation.
+constexpr int kSmemPerSm = 228 * 1024;
+constexpr int kSmemReservedPerCta = 1024;
 
 }  // namespace pkv

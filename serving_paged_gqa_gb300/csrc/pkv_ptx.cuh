@@ -15,6 +15,24 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// ---- grid dependencies (programmatic dependent launch) and CTA-subset barriers -------------------------------
+// Blocks until the grid this one was launched after (with programmatic stream serialization) has completed and its
+// memory is visible; returns at once when there is no such grid.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the grid launched after this one (with programmatic stream serialization) start its prologue.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Named barrier over `threads` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Brings a TMA descriptor (kernel-parameter address) into the descriptor cache.
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
 // ---- mbarrier -------------------------------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");

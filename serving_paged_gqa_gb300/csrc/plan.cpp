@@ -69,6 +69,10 @@ int fill_plan(const pkv_problem* pr, const int32_t* lens, int32_t num_sms, int32
     if (variant < PKV_VARIANT_SINGLE || variant > PKV_VARIANT_WORKQUEUE) return PKV_E_INVAL;
     if (ctas_per_sm <= 0) ctas_per_sm = 2;
     const int B = pr->batch, Hkv = pr->num_kv_heads, G = pr->num_q_heads / pr->num_kv_heads;
+    // never more CTAs per SM than fit in its registers and shared memory: the persistent grid is one wave
+    ctas_per_sm = std::min(ctas_per_sm, kDecodeCtasPerSm);
+    const int smem = decode_smem_bytes(G);
+    if (smem > 0) ctas_per_sm = std::max(1, std::min(ctas_per_sm, kSmemPerSm / (smem + kSmemReservedPerCta)));
     int64_t max_pages = 0, sum_len = 0;
     for (int b = 0; b < B; ++b) {
         if (lens[b] < 0 || (int64_t)lens[b] > (int64_t)pr->max_pages_per_seq * kPageSize) return PKV_E_INVAL;
@@ -102,6 +106,7 @@ int fill_plan(const pkv_problem* pr, const int32_t* lens, int32_t num_sms, int32
     plan->chunk_pages = chunk;
     plan->num_splits = (int32_t)splits;
     plan->num_tasks = (int32_t)tasks;
+    plan->fuse_merge = variant == PKV_VARIANT_SINGLE ? 0 : 1;
     plan->group = G;
     plan->num_sms = num_sms;
     plan->problem = *pr;
@@ -111,6 +116,8 @@ int fill_plan(const pkv_problem* pr, const int32_t* lens, int32_t num_sms, int32
     plan->state_capacity = variant == PKV_VARIANT_SINGLE ? 0 : tasks * G;
 
     int64_t off = kWsAlign;  // header
+    plan->off_counters = off;
+    off = align_up(off + 4 * (int64_t)B * Hkv, kWsAlign);
     plan->off_row_off = off;
     off = align_up(off + 4 * (int64_t)B, kWsAlign);
     plan->off_row_splits = off;
@@ -221,10 +228,11 @@ extern "C" int pkv_plan(const pkv_problem* pr, const int32_t* lens, int32_t num_
 
 extern "C" int pkv_plan_launches(const pkv_plan_t* plan) {
     if (!plan) return 0;
+    const int merge = plan->fuse_merge ? 0 : 1;
     switch (plan->variant) {
         case PKV_VARIANT_SINGLE: return 1;
-        case PKV_VARIANT_SPLIT: return 2;
-        case PKV_VARIANT_WORKQUEUE: return 3;
+        case PKV_VARIANT_SPLIT: return 1 + merge;
+        case PKV_VARIANT_WORKQUEUE: return 2 + merge;
         default: return 0;
     }
 }

@@ -57,13 +57,16 @@ extern "C" int pkv_decode_step_static(const pkv_plan_t* plan, const pkv_problem*
     void* ws = nullptr;
     int rc = scratch_address(&ws);
     if (rc != PKV_OK) return rc;
-    // Same validation and kernels as the caller-owned-workspace path; it enqueues nothing if it rejects.
-    rc = pkv_decode_step(plan, problem, q, k_pool, v_pool, block_table, seq_lens_dev, scale, ws,
-                         PKV_STATIC_SCRATCH_BYTES, out, stream);
-    if (rc != PKV_OK) return rc;
-    // The status word is the only part of the array a step reads before writing it: hand it over, then clear it
-    // so the next call starts from zero.
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Same validation and kernels as the caller-owned-workspace path, all validated before anything is enqueued.
+    // The fused merge's arrival counters must start at zero: a completed step leaves them at zero, but a step
+    // that gave up (a timeout, a truncated task list) may not, and no caller can re-initialise this array, so
+    // every call clears them first.
+    rc = decode_step(plan, problem, q, k_pool, v_pool, block_table, seq_lens_dev, scale, ws, PKV_STATIC_SCRATCH_BYTES,
+                     out, stream, true);
+    if (rc != PKV_OK) return rc;
+    // The status word is the only other part of the array a step reads before writing it: hand it over, then
+    // clear it so the next call starts from zero.
     uint32_t* status = &static_cast<pkv_ws_header*>(ws)->status;
     if (status_dev &&
         cudaMemcpyAsync(status_dev, status, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)

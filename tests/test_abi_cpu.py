@@ -41,7 +41,7 @@ def test_exports_every_declared_symbol():
 
 
 def test_version_and_errors():
-    assert pkv.pkv_version() == 1
+    assert pkv.pkv_version() == 2
     assert "null" in pkv.pkv_strerror(-3)
     assert pkv.pkv_strerror(0) == "ok"
 
@@ -73,13 +73,32 @@ def test_plan_fixed_counts_match_oracle_worklist():
         assert sp.num_splits == S and sp.num_tasks == 8 * 8 * S
         for pl in (wq, sp):
             assert pl.grid_ctas == min(pl.num_tasks, 2 * 152)
-            offs = [pl.off_row_off, pl.off_row_splits, pl.off_tasks, pl.off_ml, pl.off_acc, pl.ws_bytes]
+            offs = [pl.off_counters, pl.off_row_off, pl.off_row_splits, pl.off_tasks, pl.off_ml, pl.off_acc,
+                    pl.ws_bytes]
             assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
             assert pl.off_acc + 4 * 128 * pl.state_capacity <= pl.ws_bytes
+            assert pl.off_counters == 256 and pl.off_counters + 4 * 8 * 8 <= pl.off_row_off
             assert abs(pl.kv_bytes - (4096 * int(lens.sum()) + 16384 * 8)) < 1
+            assert pl.fuse_merge == 1
+        assert pkv.pkv_plan_launches(wq) == 2 and pkv.pkv_plan_launches(sp) == 1
+        wq.fuse_merge = 0
+        sp.fuse_merge = 0
+        assert pkv.pkv_plan_launches(wq) == 3 and pkv.pkv_plan_launches(sp) == 2
     single = pkv.pkv_plan_fixed(pr, lens, 152, pkv.PKV_VARIANT_SINGLE)
     assert single.num_tasks == 64 and single.num_splits == 1 and single.state_capacity == 0
-    assert pkv.pkv_plan_launches(single) == 1
+    assert single.fuse_merge == 0 and pkv.pkv_plan_launches(single) == 1
+
+
+def test_grid_is_one_wave_of_resident_ctas():
+    """The persistent grid never holds more CTAs than the SMs' shared memory keeps resident: two per SM for group
+    sizes up to 8, one for G = 16, whose per-CTA shared memory is above half of an SM's 228 KB."""
+    lens = np.full(8, 20000, dtype=np.int32)
+    for hq, hkv, per_sm in ((32, 8, 2), (32, 32, 2), (64, 8, 2), (128, 8, 1), (16, 1, 1)):
+        pr = pkv.make_problem(8, hq, hkv, 128, 16, 1 << 16, 2048)
+        pl = pkv.pkv_plan_fixed(pr, lens, 152, pkv.PKV_VARIANT_WORKQUEUE, 4)
+        assert pl.grid_ctas == min(pl.num_tasks, per_sm * 152), (hq, hkv, pl.grid_ctas)
+        pl = pkv.pkv_plan_fixed(pr, lens, 152, pkv.PKV_VARIANT_SPLIT, 4, ctas_per_sm=4)
+        assert pl.grid_ctas == min(pl.num_tasks, per_sm * 152)
 
 
 def test_plan_rejects_bad_input():

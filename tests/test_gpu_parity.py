@@ -275,3 +275,80 @@ def test_api_rejects_bad_arguments_before_launch():
     with pytest.raises(pkv.PkvError) as e:
         pkv.pkv_decode_step(plan, step.problem, mis, step.k, step.v, step.bt, step.lens, step.scale, ws, out)
     assert e.value.code == -5
+
+
+# ------------------------------------------------------------------------------------------- fused vs separate merge
+def _with_merge(plan, fused: int):
+    plan.fuse_merge = fused
+    return plan
+
+
+@pytest.mark.parametrize("name,seed,t", [
+    ("tiny", 3, 0), ("b1_bucketed", 7, 40), ("b8_bimodal", 8, 12), ("b8_uniform", 9, 63), ("b8_zipf", 6, 5),
+    ("b4_bimodal", 7, 30),
+])
+def test_fused_and_separate_merge_match_oracle(name, seed, t):
+    """Every config: the merge fused into the decode's last task and the separate merge kernel both match the
+    oracle, for the rectangular split grid and the workqueue, at several split sizes."""
+    tr = make_trace(name, seed, steps=t + 1)
+    step = Step(tr, t)
+    ref = step.reference()
+    pmax = int(tr.pages(t).max())
+    outs = []
+    for variant, chunk in ((SPLIT, 1), (SPLIT, max(1, -(-pmax // 19))), (WQ, 2), (WQ, 16), (WQ, 64)):
+        for fused in (1, 0):
+            plan = _with_merge(step.plan(variant, chunk), fused)
+            assert pkv.pkv_plan_launches(plan) == (1 if variant == SPLIT else 2) + (1 - fused)
+            out, _, status = step.run(plan)
+            assert status == 0, status
+            assert_close(out, ref, f"{name} seed {seed} step {t} variant {variant} c={chunk} fused={fused}")
+            outs.append(out.float())
+    for o in outs[1:]:
+        assert (o - outs[0]).abs().max().item() < 2e-3
+
+
+def test_workqueue_decode_runs_twice_on_one_build():
+    """The last CTA to finish claiming re-arms the queue head, so a second pkv_decode on the same list repeats the
+    step (fused merge: the arrival counters are back at zero as well)."""
+    step = Step(make_trace("b8_bimodal", 5, steps=1), 0)
+    ref = step.reference()
+    plan = step.plan(WQ, 8)
+    ws = pkv.alloc_workspace(plan.ws_bytes)
+    pkv.pkv_build_worklist(plan, step.problem, step.lens, ws)
+    for call in range(3):
+        out = torch.full_like(step.q, float("nan"))
+        pkv.pkv_decode(plan, step.problem, step.q, step.k, step.v, step.bt, step.lens, step.scale, ws, out)
+        torch.cuda.synchronize()
+        assert_close(out, ref, f"decode call {call} on one build")
+    assert pkv.pkv_read_status(ws) == 0
+    hdr = ws[:16].view(torch.int32).cpu().numpy()
+    assert hdr[0] == 0 and hdr[3] == 0  # queue head and finished-CTA count re-armed
+    counters = ws[plan.off_counters:plan.off_counters + 4 * 64].view(torch.int32).cpu().numpy()
+    assert not counters.any()
+
+
+def test_rows_longer_than_the_plan_raise_the_tasks_status():
+    """A plan made from shorter lengths than the device holds: the split grid's last split and the workqueue list
+    cannot cover the grown row, and both say so in the status word instead of returning silently."""
+    step = Step(_Lens([100, 300]).trace, 0)
+    short = np.array([100, 250], dtype=np.int32)
+    for variant in (SPLIT, WQ):
+        plan = pkv.pkv_plan_fixed(step.problem, short, step.sms, variant, 4)
+        _, ws, status = step.run(plan)
+        assert status & pkv.PKV_STATUS_TASKS, (variant, status)
+    # the same plans on lengths they cover are clean
+    step2 = Step(_Lens([100, 250]).trace, 0)
+    for variant in (SPLIT, WQ):
+        plan = pkv.pkv_plan_fixed(step2.problem, short, step2.sms, variant, 4)
+        out, _, status = step2.run(plan)
+        assert status == 0
+        assert_close(out, step2.reference(), f"covered lengths, variant {variant}")
+
+
+def test_all_rows_empty_write_zero_outputs():
+    step = Step(_Lens([0, 0, 0]).trace, 0)
+    for variant in (SINGLE, SPLIT, WQ):
+        for fused in (1, 0):
+            plan = _with_merge(step.plan(variant, 2), fused if variant != SINGLE else 0)
+            out, _, status = step.run(plan)
+            assert status == 0 and not out.isnan().any() and not out.any(), (variant, fused)
