@@ -1,17 +1,21 @@
 """Decode-step benchmark: paged GQA decode attention on one GB300 per rank.
 
-One step = one decode step of the trace (plan, worklist build when the plan uses the workqueue, decode, merge)
-over one batch of synthetic inputs. Default workload: the B1 bucketed long-context trace (B=1, Hq=32, Hkv=8, d=128,
-page size 16, fp16 ~N(0,1), start length from {4096, 8192, 16384, 32768}, 64 steps of +1 token per seed, pages
-shuffled in a 2^16-page pool) over the held-out seeds 5-9, cycled until K steps have run.
+One step = one decode step of a trace (plan, worklist build when the plan uses the workqueue, decode with the merge
+fused into it) over one batch of synthetic inputs. Headline workload: the B1 bucketed long-context trace (B=1,
+Hq=32, Hkv=8, d=128, page size 16, fp16 ~N(0,1), start length from {4096, 8192, 16384, 32768}, 64 steps of +1 token
+per seed, pages shuffled in a 2^16-page pool) over the held-out seeds 5-9. The K timed steps are spread evenly over
+all 5 x 64 steps of those traces (step j = k * 320 // K), so every length bucket the seeds drew is in the sample.
+The same is then done for the B8 bimodal, uniform and Zipf-like traces and the B4 bimodal trace (sub-results under
+"traces").
 
-Timing: every step is bracketed by CUDA events on the launching stream; the decode kernel alone by a second pair.
-Between steps an L2 flush runs outside the step's events: a 256 MiB write (larger than the 129 MB L2), then a
-256 MiB read of another buffer, so every step reads its KV from HBM, as it would after the other layers of a model
-ran, and starts with an L2 that holds no dirty lines (the write-back of the flush buffer is not charged to the step). `value` = tokens / sum of step
-times. `e2e` repeats the steps through the same C ABI from pinned host buffers: per step the host->device copies of
-q, seq_lens, the block table and the new token's K/V, the step, and the device->host copy of out, all inside the
-events. `cpu_baseline` times the fp64 oracle on the host on a bounded sample of the same trace steps.
+Timing: between steps an L2 flush runs (a 256 MiB write, then a 256 MiB read of another buffer, both larger than
+the 129 MB L2), so every step reads its KV from HBM, as it would after the other layers of a model ran. Then a GPU
+spin of --spin-us keeps the GPU busy while the host enqueues the step, so the CUDA events around the step (and
+around the decode kernel inside it) measure device time only, never a wait for the host. `value` = tokens / sum of
+step times. `e2e` repeats the same steps through the public API from pinned host buffers, timed on the host wall
+clock with a synchronize on both sides: per step one host->device copy of q, the block table, the lengths and the
+new token's K/V, the append of that K/V into its page slot, the step, and the device->host copy of out.
+`cpu_baseline` times the fp64 oracle on the host on a bounded sample of the same steps.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config b1_bucketed] ...
 Under torchrun (N > 1) every rank runs the same workload on its own GPU (replicas; no collective in the data
@@ -21,6 +25,7 @@ path); rank 0 prints one JSON line with value = tokens of all ranks / max over r
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -37,23 +42,28 @@ sys.path.insert(0, ROOT)
 METRIC = "decode tokens/s per trace and KV-read HBM GB/s as % of GB300 peak"
 L2_FLUSH_BYTES = 256 << 20
 HELD_OUT = [5, 6, 7, 8, 9]
+SUB_TRACES = ("b8_bimodal", "b8_uniform", "b8_zipf", "b4_bimodal")
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_kernel_b1_bucketed.md")
 
 
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3200)
+    ap.add_argument("--steps", type=int, default=64)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="b1_bucketed")
+    ap.add_argument("--traces", default=",".join(SUB_TRACES), help="sub-result traces ('none' to skip)")
     ap.add_argument("--seeds", default=",".join(map(str, HELD_OUT)))
     ap.add_argument("--variant", choices=["auto", "single", "split", "workqueue"], default="auto")
     ap.add_argument("--chunk", type=int, default=0, help="pages per split for a forced variant")
+    ap.add_argument("--separate-merge", action="store_true", help="use the merge kernel instead of the fused merge")
+    ap.add_argument("--spin-us", type=float, default=150.0, help="GPU spin before each timed step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-wall", action="store_true")
     ap.add_argument("--pool-pages", type=int, default=0, help="override the page-pool size (small profiling runs)")
     ap.add_argument("--reference-budget", type=float, default=120.0, help="seconds for the reference arm's steps")
     return ap.parse_args(argv)
@@ -76,7 +86,7 @@ def kernel_source_hash() -> str:
 
 
 def profile_traffic():
-    """(dram bytes per token of KV, kernel hash) from the committed ncu summary, if present."""
+    """(DRAM bytes per KV token, kernel hash) from the committed ncu summary, if present."""
     if not os.path.exists(PROFILE_SUMMARY):
         return None, None
     vals = {}
@@ -99,6 +109,11 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def strided(n: int, k: int) -> list[int]:
+    """k step indices spread evenly over n steps."""
+    return [(i * n) // k for i in range(k)]
+
+
 class ClockSampler:
     """nvidia-smi clocks/throttle sampler (200 ms) around the timed region."""
 
@@ -108,9 +123,6 @@ class ClockSampler:
 
     def __init__(self, gpu_index: int, enabled: bool = True):
         self.proc = None
-        self.gpu_index = gpu_index
-        self.lines = []
-        self.t_start = self.t_stop = None
         if enabled:
             try:
                 self.proc = subprocess.Popen(
@@ -118,12 +130,6 @@ class ClockSampler:
                      "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             except OSError:
                 self.proc = None
-
-    def mark_start(self):
-        self.t_start = time.time()
-
-    def mark_stop(self):
-        self.t_stop = time.time()
 
     def finish(self):
         if self.proc is None:
@@ -161,80 +167,192 @@ class L2Flush:
 
 
 # ------------------------------------------------------------------------------------------------ workload
-def build_workload(config: str, seeds, dev, pool_pages: int = 0):
-    """Device tensors for every step of every trace: pools with all pages a trace will use, per-step q, block
-    table and lengths. Returns a list of step records."""
-    import torch
+class Workload:
+    """Device tensors for every step of every seed's trace: a pool per seed holding every page the trace uses,
+    per-step q, block table and lengths."""
 
-    from workloads import make_trace
+    def __init__(self, torch, config: str, seeds, dev, pool_pages: int = 0):
+        from workloads import make_trace
 
-    steps = []
-    traces = []
-    for seed in seeds:
-        tr = make_trace(config, seed, pool_pages=pool_pages or None)
-        ps, hkv, d = tr.ps, tr.hkv, tr.d
-        k = torch.empty((tr.num_pages, ps, hkv, d), dtype=torch.float16, device=dev)
-        v = torch.empty((tr.num_pages, ps, hkv, d), dtype=torch.float16, device=dev)
-        idx = torch.from_numpy(tr.used_pages).to(dev)
-        k.index_copy_(0, idx, torch.from_numpy(tr.k_pages).to(dev))
-        v.index_copy_(0, idx, torch.from_numpy(tr.v_pages).to(dev))
-        traces.append((tr, k, v))
-        for t in range(tr.steps):
-            lens = tr.seq_lens(t)
-            bt = tr.block_table(t)
-            q = tr.q(t)
-            # the token appended at this step: row b's newest token (index L-1) and its page/slot
-            new_phys = bt[np.arange(tr.batch), (lens - 1) // ps]
-            new_slot = (lens - 1) % ps
-            steps.append({"trace": len(traces) - 1, "t": t, "lens_host": lens, "bt_host": bt, "q_host": q,
-                          "q": torch.from_numpy(q).to(dev), "bt": torch.from_numpy(bt).to(dev),
-                          "lens": torch.from_numpy(lens).to(dev), "new_phys": new_phys, "new_slot": new_slot})
-    return traces, steps
+        self.config, self.seeds = config, list(seeds)
+        self.traces, self.steps = [], []
+        for seed in seeds:
+            tr = make_trace(config, seed, pool_pages=pool_pages or None)
+            ps, hkv, d = tr.ps, tr.hkv, tr.d
+            k = torch.empty((tr.num_pages, ps, hkv, d), dtype=torch.float16, device=dev)
+            v = torch.empty((tr.num_pages, ps, hkv, d), dtype=torch.float16, device=dev)
+            idx = torch.from_numpy(tr.used_pages).to(dev)
+            k.index_copy_(0, idx, torch.from_numpy(tr.k_pages).to(dev))
+            v.index_copy_(0, idx, torch.from_numpy(tr.v_pages).to(dev))
+            self.traces.append((tr, k, v))
+            for t in range(tr.steps):
+                lens = tr.seq_lens(t)
+                bt = tr.block_table(t)
+                q = tr.q(t)
+                self.steps.append({"trace": len(self.traces) - 1, "seed": int(seed), "t": t, "lens_host": lens,
+                                   "bt_host": bt, "q_host": q, "q": torch.from_numpy(q).to(dev),
+                                   "bt": torch.from_numpy(bt).to(dev), "lens": torch.from_numpy(lens).to(dev)})
+        tr0 = self.traces[0][0]
+        self.B, self.Hq, self.Hkv, self.d, self.ps = tr0.batch, tr0.hq, tr0.hkv, tr0.d, tr0.ps
 
-
-def decode_fit(kv_bytes, dec_ms):
-    """Least-squares fit of decode time = fixed + bytes / bandwidth over the timed steps."""
-    if len(set(np.round(kv_bytes / 1e6, 3))) < 2:
-        return None
-    slope, icpt = np.polyfit(kv_bytes, dec_ms * 1e3, 1)
-    return {"fixed_us": float(icpt), "incremental_gbs": float(1e-3 / slope) if slope > 0 else None}
+    def problem(self, pkv, i):
+        tr = self.traces[i][0]
+        return pkv.make_problem(tr.batch, tr.hq, tr.hkv, tr.d, tr.ps, tr.num_pages, tr.max_pages)
 
 
 def make_plan(pkv, problem, lens, sms, args):
     if args.variant == "auto":
-        return pkv.pkv_plan(problem, lens, sms)
-    v = {"single": pkv.PKV_VARIANT_SINGLE, "split": pkv.PKV_VARIANT_SPLIT,
-         "workqueue": pkv.PKV_VARIANT_WORKQUEUE}[args.variant]
-    chunk = args.chunk
-    if chunk <= 0:
-        pmax = int(((lens.astype(np.int64) + 15) // 16).max())
-        chunk = max(1, -(-pmax // 32))
-    return pkv.pkv_plan_fixed(problem, lens, sms, v, chunk)
+        plan = pkv.pkv_plan(problem, lens, sms)
+    else:
+        v = {"single": pkv.PKV_VARIANT_SINGLE, "split": pkv.PKV_VARIANT_SPLIT,
+             "workqueue": pkv.PKV_VARIANT_WORKQUEUE}[args.variant]
+        chunk = args.chunk
+        if chunk <= 0:
+            pmax = int(((lens.astype(np.int64) + 15) // 16).max())
+            chunk = max(1, -(-pmax // 32))
+        plan = pkv.pkv_plan_fixed(problem, lens, sms, v, chunk)
+    if args.separate_merge and plan.variant != pkv.PKV_VARIANT_SINGLE:
+        plan.fuse_merge = 0
+    return plan
+
+
+class Marshalled:
+    """ctypes arguments of one step's C calls, built before the timed region."""
+
+    def __init__(self, pkv, wl, j, plan, ws, out, scale, stream):
+        s = wl.steps[j]
+        _, kpool, vpool = wl.traces[s["trace"]]
+        self.plan = plan
+        self.problem = wl.problem(pkv, s["trace"])
+        vp = ctypes.c_void_p
+        st = vp(stream.cuda_stream)
+        pr, pl = ctypes.byref(self.problem), ctypes.byref(self.plan)
+        self.build = (pl, pr, vp(s["lens"].data_ptr()), vp(ws.data_ptr()), ws.numel(), st)
+        self.decode = (pl, pr, vp(s["q"].data_ptr()), vp(kpool.data_ptr()), vp(vpool.data_ptr()),
+                       vp(s["bt"].data_ptr()), vp(s["lens"].data_ptr()), ctypes.c_float(scale), vp(ws.data_ptr()),
+                       ws.numel(), vp(out.data_ptr()), st)
+        self.merge = (pl, pr, vp(ws.data_ptr()), ws.numel(), vp(out.data_ptr()), st)
+        self.wq = plan.variant == pkv.PKV_VARIANT_WORKQUEUE
+        self.separate_merge = plan.variant != pkv.PKV_VARIANT_SINGLE and not plan.fuse_merge
+
+
+def _call(fn, args, what):
+    rc = fn(*args)
+    if rc != 0:
+        raise SystemExit(f"{what} failed: {rc}")
+
+
+def time_workload(pkv, torch, wl, K, W, args, sms, dev, flush, stream):
+    """Times K steps spread over the workload (after W warm-up steps): events around each step and around the
+    decode kernel inside it. Returns per-step arrays and the plans used."""
+    lib = pkv.load()
+    idx = strided(len(wl.steps), K)
+    warm = strided(len(wl.steps), max(W, 1))[:W]
+    scale = 1.0 / math.sqrt(wl.d)
+    plans = {}
+    for j in set(idx) | set(warm):
+        s = wl.steps[j]
+        plans[j] = make_plan(pkv, wl.problem(pkv, s["trace"]), s["lens_host"], sms, args)
+    ws = pkv.alloc_workspace(max(p.ws_bytes for p in plans.values()), dev)
+    out = torch.empty((wl.B, wl.Hq, wl.d), dtype=torch.float16, device=dev)
+    calls = {j: Marshalled(pkv, wl, j, plans[j], ws, out, scale, stream) for j in plans}
+    spin_cycles = int(args.spin_us * 1e-6 * 2.0e9)
+
+    def step(c, ev=None, inner=False):
+        # inner events split the step into its kernels; they also stop a dependent launch from overlapping the
+        # kernel before it, so the step time is taken in a pass without them
+        if ev is not None:
+            ev[0].record(stream)
+        if c.wq:
+            _call(lib.pkv_build_worklist, c.build, "pkv_build_worklist")
+        if inner:
+            ev[1].record(stream)
+        _call(lib.pkv_decode, c.decode, "pkv_decode")
+        if inner:
+            ev[2].record(stream)
+        if c.separate_merge:
+            _call(lib.pkv_merge, c.merge, "pkv_merge")
+        if ev is not None:
+            ev[3].record(stream)
+
+    for j in warm:
+        flush()
+        step(calls[j])
+    torch.cuda.synchronize()
+    if pkv.pkv_read_status(ws) != 0:
+        raise SystemExit("device status set during warm-up")
+
+    def timed_pass(inner):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+        torch.cuda.synchronize()
+        for k, j in enumerate(idx):
+            flush()
+            torch.cuda._sleep(spin_cycles)
+            step(calls[j], ev[k], inner)
+        torch.cuda.synchronize()
+        return ev
+
+    ev = timed_pass(False)
+    launches = sum(pkv.pkv_plan_launches(plans[j]) for j in idx)
+    step_ms = np.array([e[0].elapsed_time(e[3]) for e in ev])
+    ev = timed_pass(True)
+    status = pkv.pkv_read_status(ws)
+    dec_ms = np.array([e[1].elapsed_time(e[2]) for e in ev])
+    kv_bytes = np.array([plans[j].kv_bytes for j in idx])
+    return {"idx": idx, "plans": [plans[j] for j in idx], "step_ms": step_ms, "dec_ms": dec_ms,
+            "kv_bytes": kv_bytes, "launches": launches, "status": status, "ws": ws, "out": out}
+
+
+def by_tokens(wl, r):
+    """Mean step / decode time of the timed steps grouped by the step's token count rounded to a power of two."""
+    groups = {}
+    for k, j in enumerate(r["idx"]):
+        key = str(int(2 ** round(math.log2(max(1, int(wl.steps[j]["lens_host"].sum()))))))
+        groups.setdefault(key, []).append(k)
+    return {key: {"steps": len(ks), "step_us": 1e3 * float(r["step_ms"][ks].mean()),
+                  "decode_us": 1e3 * float(r["dec_ms"][ks].mean()),
+                  "bytes": float(r["kv_bytes"][ks].mean())} for key, ks in sorted(groups.items(), key=lambda x: int(x[0]))}
+
+
+def summarize(pkv, wl, r, peak):
+    plans = r["plans"]
+    K = len(plans)
+    tok = K * wl.B
+    return {"by_tokens": by_tokens(wl, r),"tokens_per_s": tok / (r["step_ms"].sum() * 1e-3), "step_us_mean": 1e3 * float(r["step_ms"].mean()),
+            "decode_us_mean": 1e3 * float(r["dec_ms"].mean()),
+            "decode_frac": float(r["kv_bytes"].sum() / (r["dec_ms"].sum() * 1e-3)) / 1e9 / peak,
+            "step_frac": float(r["kv_bytes"].sum() / (r["step_ms"].sum() * 1e-3)) / 1e9 / peak,
+            "algorithmic_bytes_per_step": float(r["kv_bytes"].mean()),
+            "variants_used": sorted({pkv.VARIANT_NAMES[p.variant] for p in plans}),
+            "chunk_pages_min_max": [int(min(p.chunk_pages for p in plans)), int(max(p.chunk_pages for p in plans))],
+            "splits_min_max": [int(min(p.num_splits for p in plans)), int(max(p.num_splits for p in plans))],
+            "launches_per_step": r["launches"] / K, "steps": K, "device_status": int(r["status"])}
 
 
 # ------------------------------------------------------------------------------------------------ oracle legs
-def oracle_baseline(config, seeds, budget_s):
-    """Times the fp64 oracle on whole trace steps (all query heads) until the budget is spent."""
+def oracle_baseline(wl, idx, budget_s):
+    """Times the fp64 oracle on whole trace steps (all query heads) of the timed step set until the budget is
+    spent."""
     import oracle
-    from workloads import make_trace
 
+    pools = {}
     done_tokens, spent, n_steps = 0, 0.0, 0
-    for seed in seeds:
-        tr = make_trace(config, seed)
-        kp, vp = tr.host_pools()
-        for t in range(0, tr.steps, 16):
-            t0 = time.perf_counter()
-            oracle.attention(tr.q(t), kp, vp, tr.block_table(t), tr.seq_lens(t))
-            spent += time.perf_counter() - t0
-            done_tokens += tr.batch
-            n_steps += 1
-            if spent >= budget_s:
-                break
+    for j in idx:
+        s = wl.steps[j]
+        tr = wl.traces[s["trace"]][0]
+        if s["trace"] not in pools:
+            pools[s["trace"]] = tr.host_pools()
+        kp, vp = pools[s["trace"]]
+        t0 = time.perf_counter()
+        oracle.attention(s["q_host"], kp, vp, s["bt_host"], s["lens_host"])
+        spent += time.perf_counter() - t0
+        done_tokens += tr.batch
+        n_steps += 1
         if spent >= budget_s:
             break
     return {"value": done_tokens / spent, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{n_steps} full {config} trace steps (every 16th step of the held-out seeds), all "
-                      f"{make_trace(config, seeds[0]).hq} query heads per row, fp64, {spent:.1f} s"}
+            "sample": f"the first {n_steps} of the {len(idx)} timed {wl.config} steps (held-out seeds "
+                      f"{wl.seeds}), all {wl.Hq} query heads per row, fp64, {spent:.1f} s"}
 
 
 def run_reference(args):
@@ -255,9 +373,10 @@ def run_reference(args):
     order = []
     for i, (tr, _, _) in enumerate(traces):
         order += [(i, t) for t in range(tr.steps)]
+    pick = strided(len(order), args.steps)
 
     def one(k, npairs):
-        i, t = order[k % len(order)]
+        i, t = order[pick[k % len(pick)]]
         tr, kp, vp = traces[i]
         sel = pairs_all[(np.arange(npairs) + k * npairs) % len(pairs_all)]
         t0 = time.perf_counter()
@@ -269,14 +388,15 @@ def run_reference(args):
     npairs = int(max(1, min(len(pairs_all), args.reference_budget / max(1, args.steps + args.warmup) / probe)))
     for k in range(args.warmup):
         one(k, npairs)
-    spent = sum(one(args.warmup + k, npairs) for k in range(args.steps))
+    spent = sum(one(k, npairs) for k in range(args.steps))
     tokens = args.steps * npairs / (B * Hq)
     value = tokens / spent
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * spent / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": args.config, "seeds": seeds, "batch": B, "num_q_heads": Hq,
-                       "num_kv_heads": traces[0][0].hkv, "head_dim": traces[0][0].d, "page_size": traces[0][0].ps},
+                       "num_kv_heads": traces[0][0].hkv, "head_dim": traces[0][0].d, "page_size": traces[0][0].ps,
+                       "timed_steps": f"{args.steps} steps spread over the {len(order)} trace steps"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": f"{npairs} of {B * Hq} (row, query head) pairs of one trace step per step"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -284,6 +404,72 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------------------------------------ our arm
+def run_e2e(pkv, torch, wl, idx, args, sms, flush, stream, dev):
+    """The same steps through the public API from pinned host buffers, host wall clock with a synchronize on both
+    sides: one H2D copy of (q, block table, lengths, new K, new V), the append of the new token's K/V into its page
+    slot, pkv_plan + pkv_decode_step, one D2H copy of out."""
+    B, Hq, Hkv, d, ps = wl.B, wl.Hq, wl.Hkv, wl.d, wl.ps
+    scale = 1.0 / math.sqrt(d)
+    recs = []
+    for j in idx:
+        s = wl.steps[j]
+        tr = wl.traces[s["trace"]][0]
+        lens = s["lens_host"]
+        new_phys = s["bt_host"][np.arange(B), (lens - 1) // ps]
+        new_slot = (lens - 1) % ps
+        used_index = {int(p): i for i, p in enumerate(tr.used_pages)}
+        k_new = np.stack([tr.k_pages[used_index[int(new_phys[b])], int(new_slot[b])] for b in range(B)])
+        v_new = np.stack([tr.v_pages[used_index[int(new_phys[b])], int(new_slot[b])] for b in range(B)])
+        rows = (new_phys.astype(np.int64) * ps + new_slot).astype(np.int64)
+        parts = [s["q_host"].view(np.uint8).ravel(), k_new.view(np.uint8).ravel(), v_new.view(np.uint8).ravel(),
+                 s["bt_host"].view(np.uint8).ravel(), lens.view(np.uint8).ravel(), rows.view(np.uint8).ravel()]
+        # one pinned buffer, every part starting on a 256-byte boundary (the library wants 16-byte aligned q)
+        sizes = [-(-p.size // 256) * 256 for p in parts]
+        buf = np.zeros(sum(sizes), dtype=np.uint8)
+        o = np.cumsum([0] + sizes)
+        for i, part in enumerate(parts):
+            buf[o[i]:o[i] + part.size] = part
+        packed = torch.from_numpy(buf).pin_memory()
+        recs.append((j, packed, [p.size for p in parts], o))
+    nbytes_max = max(p.numel() for _, p, _, _ in recs)
+    dbuf = torch.empty(nbytes_max, dtype=torch.uint8, device=dev)
+    out_d = torch.empty((B, Hq, d), dtype=torch.float16, device=dev)
+    out_h = torch.empty((B, Hq, d), dtype=torch.float16).pin_memory()
+    # the workspace is allocated once, before the timed steps, for the largest plan among them
+    ws_bytes = max(make_plan(pkv, wl.problem(pkv, wl.steps[j]["trace"]), wl.steps[j]["lens_host"], sms, args).ws_bytes
+                   for j in idx)
+    ws = pkv.alloc_workspace(ws_bytes, dev)
+    times = []
+    h2d = d2h = 0
+    for j, packed, sizes, o in recs:
+        s = wl.steps[j]
+        tr, kpool, vpool = wl.traces[s["trace"]]
+        problem = wl.problem(pkv, s["trace"])
+        flush()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dbuf[:packed.numel()].copy_(packed, non_blocking=True)
+        part = [dbuf[o[i]:o[i] + sizes[i]] for i in range(6)]
+        q = part[0].view(torch.float16).view(B, Hq, d)
+        k_new = part[1].view(torch.float16).view(B, Hkv * d)
+        v_new = part[2].view(torch.float16).view(B, Hkv * d)
+        bt = part[3].view(torch.int32).view(B, tr.max_pages)
+        lens = part[4].view(torch.int32)
+        rows = part[5].view(torch.int64)
+        kpool.view(-1, Hkv * d).index_copy_(0, rows, k_new)
+        vpool.view(-1, Hkv * d).index_copy_(0, rows, v_new)
+        plan = make_plan(pkv, problem, s["lens_host"], sms, args)
+        pkv.pkv_decode_step(plan, problem, q, kpool, vpool, bt, lens, scale, ws, out_d, stream)
+        out_h.copy_(out_d, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+        times.append(time.perf_counter() - t0)
+        h2d = packed.numel()
+        d2h = out_h.numel() * 2
+    return {"value": B * len(times) / float(np.sum(times)), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": len(times), "us_per_step": 1e6 * float(np.mean(times)),
+            "timing": "host wall clock per step, synchronize on both sides; includes pkv_plan"}
+
+
 def run_ours(args):
     import torch
 
@@ -303,187 +489,101 @@ def run_ours(args):
     import serving_paged_gqa_gb300 as pkv
 
     seeds = [int(s) for s in args.seeds.split(",")]
-    traces, steps = build_workload(args.config, seeds, dev, args.pool_pages)
-    tr0 = traces[0][0]
-    B, Hq, Hkv, d = tr0.batch, tr0.hq, tr0.hkv, tr0.d
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    scale = 1.0 / math.sqrt(d)
-    problems = [pkv.make_problem(B, Hq, Hkv, d, tr.ps, tr.num_pages, tr.max_pages) for tr, _, _ in traces]
-
-    # plans for every trace step (host planning is timed separately, in the wall loop)
-    t0 = time.perf_counter()
-    plans = [make_plan(pkv, problems[s["trace"]], s["lens_host"], sms, args) for s in steps]
-    plan_us = 1e6 * (time.perf_counter() - t0) / len(steps)
-    ws = pkv.alloc_workspace(max(p.ws_bytes for p in plans), dev)
-    out = torch.empty((B, Hq, d), dtype=torch.float16, device=dev)
+    peak, peak_kind = measured_peaks()
     flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
+    K, W = args.steps, args.warmup
 
-    def launch(k):
-        s = steps[k % len(steps)]
-        tr, kpool, vpool = traces[s["trace"]]
-        pkv.pkv_decode_step(plans[k % len(steps)], problems[s["trace"]], s["q"], kpool, vpool, s["bt"], s["lens"],
-                            scale, ws, out, stream)
-
-    for k in range(args.warmup):
-        flush()
-        launch(k)
-    torch.cuda.synchronize()
-    if pkv.pkv_read_status(ws) != 0:
-        raise SystemExit("device status set during warm-up")
-
-    # ---- timed region: K steps, events per step and around the decode kernel
-    K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    # ---- headline workload
+    wl = Workload(torch, args.config, seeds, dev, args.pool_pages)
     clocks = ClockSampler(local, enabled=not args.no_clocks)
-    time.sleep(0.3 if not args.no_clocks else 0)
+    if not args.no_clocks:
+        time.sleep(0.3)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks.mark_start()
     wall0 = time.perf_counter()
-    launches = 0
-    for k in range(K):
-        j = (args.warmup + k) % len(steps)
-        s = steps[j]
-        tr, kpool, vpool = traces[s["trace"]]
-        plan, problem = plans[j], problems[s["trace"]]
-        flush()
-        e = ev[k]
-        e[0].record(stream)
-        if plan.variant == pkv.PKV_VARIANT_WORKQUEUE:
-            pkv.pkv_build_worklist(plan, problem, s["lens"], ws, stream)
-        e[1].record(stream)
-        pkv.pkv_decode(plan, problem, s["q"], kpool, vpool, s["bt"], s["lens"], scale, ws, out, stream)
-        e[2].record(stream)
-        pkv.pkv_merge(plan, problem, ws, out, stream)
-        e[3].record(stream)
-        launches += pkv.pkv_plan_launches(plan)
-    torch.cuda.synchronize()
-    wall_timed = time.perf_counter() - wall0
+    r = time_workload(pkv, torch, wl, K, W, args, sms, dev, flush, stream)
+    timed_wall = time.perf_counter() - wall0
     if world > 1:
         torch.distributed.barrier()
-    clocks.mark_stop()
-    step_ms = np.array([e[0].elapsed_time(e[3]) for e in ev])
-    dec_ms = np.array([e[1].elapsed_time(e[2]) for e in ev])
-    build_ms = np.array([e[0].elapsed_time(e[1]) for e in ev])
-    merge_ms = np.array([e[2].elapsed_time(e[3]) for e in ev])
-    kv_bytes = np.array([plans[(args.warmup + k) % len(steps)].kv_bytes for k in range(K)])
-    tokens = K * B
-    total_ms = float(step_ms.sum())
+    clk = clocks.finish()
+    total_ms = float(r["step_ms"].sum())
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
-    status = pkv.pkv_read_status(ws)
+    head = summarize(pkv, wl, r, peak)
 
-    # ---- synchronized wall time per step (pages' protocol): plan + launches + sync, no flush inside
-    wall = []
-    for k in range(min(K, 2 * len(steps))):
-        j = k % len(steps)
-        s = steps[j]
-        tr, kpool, vpool = traces[s["trace"]]
-        flush()
-        torch.cuda.synchronize()
-        w0 = time.perf_counter()
-        plan = make_plan(pkv, problems[s["trace"]], s["lens_host"], sms, args)
-        pkv.pkv_decode_step(plan, problems[s["trace"]], s["q"], kpool, vpool, s["bt"], s["lens"], scale, ws, out,
-                            stream)
-        torch.cuda.synchronize()
-        wall.append(time.perf_counter() - w0)
-    wall_us = 1e6 * float(np.mean(wall))
+    # ---- synchronized wall time per step (the pages' protocol): plan + launches + sync, flush outside
+    wall_us = None
+    if not args.no_wall:
+        scale = 1.0 / math.sqrt(wl.d)
+        wall = []
+        for j in r["idx"]:
+            s = wl.steps[j]
+            tr, kpool, vpool = wl.traces[s["trace"]]
+            problem = wl.problem(pkv, s["trace"])
+            flush()
+            torch.cuda.synchronize()
+            w0 = time.perf_counter()
+            plan = make_plan(pkv, problem, s["lens_host"], sms, args)
+            pkv.pkv_decode_step(plan, problem, s["q"], kpool, vpool, s["bt"], s["lens"], scale, r["ws"], r["out"],
+                                stream)
+            torch.cuda.synchronize()
+            wall.append(time.perf_counter() - w0)
+        wall_us = 1e6 * float(np.mean(wall))
 
-    # ---- e2e through the C ABI from pinned host buffers
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(args, pkv, torch, traces, steps, plans, problems, ws, flush, stream, scale, dev)
+    e2e = None if args.no_e2e else run_e2e(pkv, torch, wl, r["idx"], args, sms, flush, stream, dev)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = oracle_baseline(wl, r["idx"], args.cpu_seconds)
 
-    peak, peak_kind = measured_peaks()
-    achieved = float(kv_bytes.sum() / (dec_ms.sum() * 1e-3)) / 1e9
     traffic_per_tok, traffic_hash = profile_traffic()
     traffic = None
     if traffic_per_tok is not None and traffic_hash == kernel_source_hash():
-        mean_tokens = float(np.mean([int(steps[(args.warmup + k) % len(steps)]["lens_host"].sum())
-                                     for k in range(K)]))
+        mean_tokens = float(np.mean([int(wl.steps[j]["lens_host"].sum()) for j in r["idx"]]))
         traffic = traffic_per_tok * mean_tokens
-    clk = clocks.finish()
-
-    if rank != 0:
-        return
-    cpu = None
-    if not args.no_cpu_baseline and world >= 1:
-        cpu = oracle_baseline(args.config, seeds, args.cpu_seconds)
-    variants = sorted({pkv.VARIANT_NAMES[plans[(args.warmup + k) % len(steps)].variant] for k in range(K)})
-    splits = [plans[(args.warmup + k) % len(steps)].num_splits for k in range(K)]
+    dec_gbs = float(r["kv_bytes"].sum() / (r["dec_ms"].sum() * 1e-3)) / 1e9
+    B, Hq, Hkv, d = wl.B, wl.Hq, wl.Hkv, wl.d
+    config = {"workload": args.config, "seeds": seeds, "batch": B, "num_q_heads": Hq, "num_kv_heads": Hkv,
+              "head_dim": d, "page_size": wl.ps, "pool_pages": wl.traces[0][0].num_pages,
+              "trace_steps": len(wl.steps),
+              "timed_steps": f"{K} steps spread evenly over all {len(wl.steps)} steps of the seeds' traces",
+              "l2": "flushed between steps outside the step events (256 MiB write, then 256 MiB read); "
+                    f"a {args.spin_us:.0f} us GPU spin before each step keeps host enqueue out of the events",
+              "variant": args.variant, "merge": "separate kernel" if args.separate_merge else "fused",
+              "variants_used": head["variants_used"], "chunk_pages_min_max": head["chunk_pages_min_max"],
+              "splits_min_max": head["splits_min_max"], "parallelism": f"replicas x{world}"}
     line = {
-        "metric": METRIC, "value": tokens * world / (total_ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
-        "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16 in, f32 accumulate", "data": "synthetic",
-        "impl": "ours",
-        "config": {"workload": args.config, "seeds": seeds, "batch": B, "num_q_heads": Hq, "num_kv_heads": Hkv,
-                   "head_dim": d, "page_size": tr0.ps, "pool_pages": tr0.num_pages, "trace_steps": len(steps),
-                   "l2": "flushed between steps outside the step events (256 MiB write, then 256 MiB read)",
-                   "variant": args.variant, "variants_used": variants,
-                   "splits_min_max": [int(min(splits)), int(max(splits))], "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "kernel": "pkv decode_kernel", "peak_source": f"hbm_gbs ({peak_kind})",
-                     "algorithmic_bytes_per_step": float(kv_bytes.mean())},
-        "decode_us_mean": 1e3 * float(dec_ms.mean()), "step_us_mean": 1e3 * float(step_ms.mean()),
-        "build_us_mean": 1e3 * float(build_ms.mean()), "merge_us_mean": 1e3 * float(merge_ms.mean()),
-        "decode_fit": decode_fit(kv_bytes, dec_ms),
-        "step_us_p50": 1e3 * float(np.median(step_ms)), "kv_gbs_step": float(kv_bytes.sum() / (step_ms.sum() * 1e-3)) / 1e9,
-        "wall_us_per_step": wall_us, "wall_tokens_per_s": B / (wall_us * 1e-6), "plan_us": plan_us,
-        "timed_wall_s": wall_timed, "gpu_launches": launches, "device_status": status,
+        "metric": METRIC, "value": K * B * world / (total_ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic", "impl": "ours", "config": config,
+        "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peak, "unit": "GB/s", "frac": dec_gbs / peak,
+                     "traffic": traffic, "kernel": "pkv decode_kernel (merge fused)",
+                     "peak_source": f"hbm_gbs ({peak_kind})",
+                     "algorithmic_bytes_per_launch": head["algorithmic_bytes_per_step"]},
+        "decode_us_mean": head["decode_us_mean"], "step_us_mean": head["step_us_mean"],
+        "step_frac": head["step_frac"], "launches_per_step": head["launches_per_step"], "by_tokens": head["by_tokens"],
+        "wall_us_per_step": wall_us, "wall_tokens_per_s": None if wall_us is None else B / (wall_us * 1e-6),
+        "timed_wall_s": timed_wall, "gpu_launches": r["launches"], "device_status": int(r["status"]),
         "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
     }
-    print(json.dumps(line), flush=True)
+    del wl, r
 
-
-def run_e2e(args, pkv, torch, traces, steps, plans, problems, ws, flush, stream, scale, dev):
-    """Steps through the C ABI with pinned host inputs/outputs; the copies are inside the events."""
-    B = traces[0][0].batch
-    nsteps = min(args.steps, len(steps))
-    host = []
-    for s in steps[:nsteps]:
-        tr, kpool, vpool = traces[s["trace"]]
-        ps = tr.ps
-        rows = np.arange(tr.batch)
-        # K/V of each row's newest token: [B, Hkv, d] from the trace's page contents
-        used_index = {int(p): i for i, p in enumerate(tr.used_pages)}
-        k_new = np.stack([tr.k_pages[used_index[int(s["new_phys"][b])], int(s["new_slot"][b])] for b in rows])
-        v_new = np.stack([tr.v_pages[used_index[int(s["new_phys"][b])], int(s["new_slot"][b])] for b in rows])
-        host.append({"q": torch.from_numpy(s["q_host"]).pin_memory(), "bt": torch.from_numpy(s["bt_host"]).pin_memory(),
-                     "lens": torch.from_numpy(s["lens_host"]).pin_memory(),
-                     "k_new": torch.from_numpy(k_new).pin_memory(), "v_new": torch.from_numpy(v_new).pin_memory()})
-    out_host = torch.empty((B, traces[0][0].hq, traces[0][0].d), dtype=torch.float16).pin_memory()
-    q_d = torch.empty_like(steps[0]["q"])
-    bt_d = [torch.empty((B, tr.max_pages), dtype=torch.int32, device=dev) for tr, _, _ in traces]
-    lens_d = torch.empty((B,), dtype=torch.int32, device=dev)
-    out_d = torch.empty_like(q_d)
-    times, h2d, d2h = [], 0, 0
-    for k in range(nsteps):
-        s, hs = steps[k], host[k]
-        tr, kpool, vpool = traces[s["trace"]]
-        plan = plans[k]
-        flush()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        q_d.copy_(hs["q"], non_blocking=True)
-        bt_view = bt_d[s["trace"]]
-        bt_view.copy_(hs["bt"], non_blocking=True)
-        lens_d.copy_(hs["lens"], non_blocking=True)
-        for b in range(tr.batch):  # append the new token's K and V into its page slot
-            kpool[int(s["new_phys"][b]), int(s["new_slot"][b])].copy_(hs["k_new"][b], non_blocking=True)
-            vpool[int(s["new_phys"][b]), int(s["new_slot"][b])].copy_(hs["v_new"][b], non_blocking=True)
-        pkv.pkv_decode_step(plan, problems[s["trace"]], q_d, kpool, vpool, bt_view, lens_d, scale, ws, out_d, stream)
-        out_host.copy_(out_d, non_blocking=True)
-        e1.record(stream)
-        e1.synchronize()
-        times.append(e0.elapsed_time(e1))
-        h2d = hs["q"].numel() * 2 + hs["bt"].numel() * 4 + hs["lens"].numel() * 4 + 2 * hs["k_new"].numel() * 2
-        d2h = out_host.numel() * 2
-    return {"value": B * nsteps / (1e-3 * float(np.sum(times))), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": nsteps, "us_per_step": 1e3 * float(np.mean(times))}
+    # ---- sub-results on the other traces (same protocol)
+    subs = {}
+    names = [] if args.traces in ("", "none") else [t for t in args.traces.split(",") if t != args.config]
+    for name in names:
+        torch.cuda.empty_cache()
+        wl = Workload(torch, name, seeds, dev, args.pool_pages)
+        r = time_workload(pkv, torch, wl, K, W, args, sms, dev, flush, stream)
+        subs[name] = summarize(pkv, wl, r, peak)
+        del wl, r
+    line["traces"] = subs
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 def main(argv=None):

@@ -8,26 +8,29 @@
 // splitting into partial online-softmax states combined exactly ("Sequentie Splitting"), row-local bounds with
 // neutral states for empty splits ("Row-Local Bounds"), compact workqueue ("Compact Workqueue")).
 //
-// CTA layout (persistent over tasks; grid = resident CTAs):
-//   warp NCW+1  scheduler: takes tasks (split / single: a static stride over the task space, KV heads fastest, so the
+// CTA layout (persistent over tasks; grid = one wave of resident CTAs):
+//   warp NCW+2  scheduler: takes tasks (split / single: a static stride over the task space, KV heads fastest, so the
 //               CTAs that start together read the same pages; workqueue: an atomic queue head over the built list,
 //               after waiting for the builder grid), fetches the row length and the task's first 32 block-table
 //               entries together, publishes both in a shared-memory task slot, then bulk-copies the G query rows of
 //               the task into the slot (completion on a separate barrier, so the loader never waits for q);
-//   warp NCW    loader: per page, one elected lane issues four 3-D TMA tensor copies (K and V of KV head h, each as
+//   warp NCW+1  loader: per page, one elected lane issues four 3-D TMA tensor copies (K and V of KV head h, each as
 //               two 64-column boxes of the page's 16 token rows, 128-byte swizzled) into a ring stage, counted in
 //               bytes on the stage's mbarrier; block-table entries past the slot's 32 are read one chunk ahead;
 //   warps 0..NCW-1 consumers: page j of the CTA's page sequence (counted across tasks) lives in stage j % NS and
-//               goes to warp j % NCW (NS % NCW == 0, so a stage always has the same consumer). Per page: S = Q K^T on
-//               mma.sync m16n8k16 (rows = the G query heads, columns = the 16 tokens), masking of slots past the row
-//               length, online softmax in base 2 in registers with quad shuffles, O += P V on mma.sync. At the end
-//               of a task the NCW warps combine their states through shared memory and write the normalised fp16
-//               output (single pass) or the partial state (m, l, acc) of each query head. With the merge fused, the
-//               task then counts itself in the (b, h) arrival counter; the last of the S_b tasks of (b, h) to arrive
-//               reads all S_b states from L2 and writes the merged output, then re-arms the counter. Nobody waits.
+//               goes to warp j % NCW (NS % NCW == 0, so a stage always has the same consumer). The products are
+//               taken transposed, so the 16 tokens (scores) and the head dimension (output) fill the 16-row side of
+//               mma.sync m16n8k16 and the G query heads the 8-column side: S^T = K Q^T (8 MMAs per page for G <= 8),
+//               masking of slots past the row length, online softmax in base 2 per head column, P^T rebuilt in the
+//               B-operand layout with four shuffles, O^T += V^T P^T (8 MMAs). At the end of a task each warp hands
+//               its (m, l, O) to the epilogue warp through a double-buffered shared-memory slot and moves on.
+//   warp NCW    epilogue: combines the NCW warps' partials of a task and writes the normalised output (single pass)
+//               or the partial state (m, l, acc) of each query head. With the merge fused it then counts the task
+//               in the (b, h) arrival counter; the last of the S_b tasks of (b, h) to arrive bulk-copies the S_b * G
+//               states of (b, h) from L2 through a two-buffer shared-memory chunk ring, merges them exactly and
+//               writes out, then re-arms the counter. Nobody waits for another CTA.
 // Every wait is bounded (global timer); on timeout the kernel sets PKV_STATUS_TIMEOUT in the workspace, the other
-// warps see an abort flag, the loader and the scheduler wait (bounded) for their own copies in flight, and the CTA
-// returns.
+// warps see an abort flag, every warp that issued bulk copies waits (bounded) for them, and the CTA returns.
 #include <cuda_fp16.h>
 
 #include "pkv_internal.h"
@@ -38,8 +41,9 @@ namespace {
 
 constexpr int kBoxBytes = kPageSize * 128;   // one TMA box: 16 token rows x 64 fp16 columns (128 B, swizzled)
 constexpr int kStageBytes = 4 * kBoxBytes;   // K columns 0-63, K 64-127, V 0-63, V 64-127
-constexpr int kCombRow = kHeadDim + 8;       // floats per combined row (padding against bank conflicts)
+constexpr int kCombRow = kHeadDim + 4;       // floats per partial output row (132: rows land 4 banks apart)
 constexpr int kSlotEntries = 32;             // block-table entries the scheduler prefetches per task
+constexpr int kMergeChunk = 16;              // partial states per merge chunk (8 KB of acc)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -50,17 +54,26 @@ struct TaskSlot {
     int32_t ent[kSlotEntries];              // physical page of logical page page_begin + i (i < min(npages, 32))
 };
 
+// What the epilogue warp needs to know about a task (written by consumer warp 0; npages < 0 ends the CTA).
+struct EpiHeader {
+    int32_t b, h, s, task, nsplit, npages, pad0, pad1;
+};
+
 template <int G, int NCW, int NS, int NTS>
 struct Layout {
+    static constexpr int kNT = (G + 7) / 8;  // 8-head column tiles of the MMAs
     static constexpr int kQRowsBytes = ((G * kRowBytes + 127) / 128) * 128;
+    static constexpr int kCombFloats = NCW * G * kCombRow;  // one slot: every consumer warp's O rows
+    static constexpr int kMergeBufs = G <= 4 ? 3 : 2;       // merge chunks in flight (what two CTAs' shared memory allows)
     static constexpr int off_stage = 0;  // 1024-byte aligned (128-byte swizzle atom)
     static constexpr int off_q = off_stage + NS * kStageBytes;
-    static constexpr int off_comb = off_q + NTS * kQRowsBytes;
-    static constexpr int comb_o_floats = NCW * G * kCombRow;
-    static constexpr int off_comb_ml = off_comb + comb_o_floats * 4;
-    static constexpr int off_slots = off_comb_ml + NCW * G * 8;
+    static constexpr int off_mbuf = off_q + NTS * kQRowsBytes;             // 2 merge chunks (bulk copy targets)
+    static constexpr int off_comb = off_mbuf + kMergeBufs * kMergeChunk * kHeadDim * 4;
+    static constexpr int off_comb_ml = off_comb + 2 * kCombFloats * 4;    // float2 (m, l) per slot/warp/head
+    static constexpr int off_ehdr = off_comb_ml + 2 * NCW * G * 8;
+    static constexpr int off_slots = off_ehdr + 2 * (int)sizeof(EpiHeader);
     static constexpr int off_bars = ((off_slots + NTS * (int)sizeof(TaskSlot) + 15) / 16) * 16;
-    static constexpr int nbars = 2 * NS + 3 * NTS + 4;
+    static constexpr int nbars = 2 * NS + 3 * NTS + 4 + kMergeBufs;
     static constexpr int off_flag = off_bars + nbars * 8;
     static constexpr int used = off_flag + 16;
     static constexpr int total = used + 1024;  // slack to align the base to 1024 bytes
@@ -116,56 +129,93 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-// Exact log-sum-exp merge of the nsplit partial states of query head g of the task group starting at task `first`:
-// out = sum_s e^(m_s - M) acc_s / sum_s e^(m_s - M) l_s over states with l_s > 0 (running maximum, so the states
-// are read once). Lane k owns dimensions 4k..4k+3. States were written by other CTAs: read them from L2.
-template <int G>
-__device__ __forceinline__ void merge_group(const DecodeParams& p, int first, int nsplit, int g, int lane,
-                                            __half* out_row) {
-    const float2* mlp = reinterpret_cast<const float2*>(p.ml);
-    const float4* accp = reinterpret_cast<const float4*>(p.acc);
-    float M = -INFINITY, D = 0.f;
-    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < nsplit; s0 += 8) {
-        float2 ml[8];
-        float4 av[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (s0 + j < nsplit) {
-                const size_t st = (size_t)(first + s0 + j) * G + g;
-                ml[j] = __ldcg(mlp + st);
-                av[j] = __ldcg(accp + st * (kHeadDim / 4) + lane);
-            } else {
-                ml[j] = make_float2(-INFINITY, 0.f);
-                av[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (ml[j].y > 0.f) {
-                const float m2 = ml[j].x * kLog2e;
-                const float mn = fmaxf(M, m2);
-                const float fo = fast_exp2(M - mn), fn = fast_exp2(m2 - mn);
-                D = D * fo + fn * ml[j].y;
-                A.x = A.x * fo + fn * av[j].x;
-                A.y = A.y * fo + fn * av[j].y;
-                A.z = A.z * fo + fn * av[j].z;
-                A.w = A.w * fo + fn * av[j].w;
-                M = mn;
-            }
-        }
-    }
-    const float inv = D > 0.f ? 1.f / D : 0.f;
+__device__ __forceinline__ void store_half4(__half* dst, float4 v, float scale) {
     uint2 pk;
-    pk.x = pack_half2(A.x * inv, A.y * inv);
-    pk.y = pack_half2(A.z * inv, A.w * inv);
-    *reinterpret_cast<uint2*>(out_row + lane * 4) = pk;
+    pk.x = pack_half2(v.x * scale, v.y * scale);
+    pk.y = pack_half2(v.z * scale, v.w * scale);
+    *reinterpret_cast<uint2*>(dst) = pk;
 }
 
+// ---------------------------------------------------------------------------------------------- epilogue warp
+// Exact log-sum-exp merge of the nsplit partial states of every query head of the task group starting at task
+// `first`: out_g = sum_s e^(m_s - M) acc_s / sum_s e^(m_s - M) l_s over states with l_s > 0, with a running maximum
+// so the states are read once. The states of (b, h) are contiguous ((s, g) order, g fastest); they were written by
+// other CTAs, so they are fetched through the async proxy after the acquiring fences. Lane k owns dims 4k..4k+3.
+template <int G, int NCH>
+__device__ __forceinline__ bool merge_pair(const DecodeParams& p, int first, int nsplit, __half* out_pair,
+                                           float* mbuf, uint64_t* mbar, uint32_t& missued, uint32_t& mwaited,
+                                           const WaitCtx& ctx, int lane) {
+    constexpr int kSplitsPerChunk = kMergeChunk / G;  // a chunk holds whole splits (G divides 16)
+    const float2* mlp = reinterpret_cast<const float2*>(p.ml);
+    const size_t base = (size_t)first * G;
+    const int n = nsplit * G;
+    const int nchunks = (n + kMergeChunk - 1) / kMergeChunk;
+    float M[G], D[G];
+    float4 A[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        M[g] = -INFINITY;
+        D[g] = 0.f;
+        A[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    auto issue = [&](int c) {
+        const int cnt = min(kMergeChunk, n - c * kMergeChunk);
+        const uint32_t buf = missued % NCH;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&mbar[buf], cnt * kHeadDim * 4);
+            bulk_g2s(mbuf + buf * kMergeChunk * kHeadDim, p.acc + (base + (size_t)c * kMergeChunk) * kHeadDim,
+                     cnt * kHeadDim * 4, &mbar[buf]);
+        }
+        ++missued;
+    };
+    for (int c = 0; c < min(NCH, nchunks); ++c) issue(c);
+    for (int c = 0; c < nchunks; ++c) {
+        const int cnt = min(kMergeChunk, n - c * kMergeChunk);
+        const float2 ml = lane < cnt ? __ldcg(mlp + base + (size_t)c * kMergeChunk + lane) : make_float2(0.f, 0.f);
+        const uint32_t buf = mwaited % NCH;
+        if (!warp_wait(&mbar[buf], (mwaited / NCH) & 1u, ctx)) return false;
+        ++mwaited;
+        const float* chunk = mbuf + buf * kMergeChunk * kHeadDim;
+        for (int j = 0; j < kSplitsPerChunk && j * G < cnt; ++j) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const int lj = j * G + g;
+                const float m2 = __shfl_sync(0xffffffffu, ml.x, lj) * kLog2e;
+                const float l = __shfl_sync(0xffffffffu, ml.y, lj);
+                const float4 v = *reinterpret_cast<const float4*>(chunk + lj * kHeadDim + lane * 4);
+                if (l > 0.f) {
+                    const float mn = fmaxf(M[g], m2);
+                    const float fo = fast_exp2(M[g] - mn), fn = fast_exp2(m2 - mn);
+                    D[g] = D[g] * fo + fn * l;
+                    A[g].x = A[g].x * fo + fn * v.x;
+                    A[g].y = A[g].y * fo + fn * v.y;
+                    A[g].z = A[g].z * fo + fn * v.z;
+                    A[g].w = A[g].w * fo + fn * v.w;
+                    M[g] = mn;
+                }
+            }
+        }
+        __syncwarp();
+        if (c + NCH < nchunks) {
+            fence_proxy_async_smem();  // the buffer's generic reads are done before the next copy overwrites it
+            issue(c + NCH);
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+        store_half4(out_pair + (size_t)g * kHeadDim + lane * 4, A[g], D[g] > 0.f ? 1.f / D[g] : 0.f);
+    return true;
+}
+
+// Resident CTAs per SM the kernel is compiled for: two up to G = 4; one for G >= 8, whose partial-output slots do
+// not leave room for a second CTA's shared memory.
+constexpr int ctas_per_sm(int group) { return group >= 8 ? 1 : kDecodeCtasPerSm; }
+
 template <int G, int NCW, int NS, int NTS>
-__global__ void __launch_bounds__((NCW + 2) * 32, kDecodeCtasPerSm) decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(const __grid_constant__ DecodeParams p) {
     static_assert(NS % NCW == 0, "each ring stage must map to one consumer warp");
     using L = Layout<G, NCW, NS, NTS>;
+    constexpr int kNT = L::kNT;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
     const int warp = threadIdx.x >> 5;
@@ -177,13 +227,14 @@ __global__ void __launch_bounds__((NCW + 2) * 32, kDecodeCtasPerSm) decode_kerne
     uint64_t* tmeta = bars + 2 * NS;  // task slot published (row, pages, block-table entries)
     uint64_t* tq = tmeta + NTS;       // the slot's query rows have landed
     uint64_t* tempty = tq + NTS;      // the slot has been read by the loader and every consumer
-    uint64_t* cfull = tempty + NTS;
-    uint64_t* cempty = cfull + 1;
-    uint64_t* mstate = cempty + 1;    // fused merge: every consumer warp has stored its part of the task's states
-    uint64_t* mlast = mstate + 1;     // fused merge: warp 0 has counted the task and published whether it was last
+    uint64_t* efull = tempty + NTS;   // [2] every consumer warp has written its partial of the task into the slot
+    uint64_t* eempty = efull + 2;     // [2] the epilogue warp has read the slot
+    uint64_t* mbar = eempty + 2;      // [kMergeBufs] merge chunk landed
     TaskSlot* slots = reinterpret_cast<TaskSlot*>(smem + L::off_slots);
+    EpiHeader* ehdr = reinterpret_cast<EpiHeader*>(smem + L::off_ehdr);
+    float* comb_o = reinterpret_cast<float*>(smem + L::off_comb);
+    float2* comb_ml = reinterpret_cast<float2*>(smem + L::off_comb_ml);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_flag);
-    volatile int* last_flag = abort_flag + 1;
     const WaitCtx ctx{abort_flag, &p.hdr->status};
 
     if (threadIdx.x == 0) {
@@ -196,19 +247,22 @@ __global__ void __launch_bounds__((NCW + 2) * 32, kDecodeCtasPerSm) decode_kerne
             mbar_init(&tq[i], 1);
             mbar_init(&tempty[i], NCW + 1);
         }
-        mbar_init(cfull, NCW);
-        mbar_init(cempty, NCW);
-        mbar_init(mstate, NCW);
-        mbar_init(mlast, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&efull[i], NCW);
+            mbar_init(&eempty[i], 1);
+        }
+        for (int i = 0; i < L::kMergeBufs; ++i) mbar_init(&mbar[i], 1);
         *abort_flag = 0;
-        *last_flag = 0;
         mbar_fence_init();
     }
     __syncthreads();
+    // A separate merge grid launched after this one waits for its completion before reading anything; it may be
+    // scheduled now and sit resident beside this grid.
+    grid_launch_dependents();
 
     const int Hq = p.Hq, Hkv = p.Hkv;
 
-    if (warp == NCW + 1) {
+    if (warp == NCW + 2) {
         // ------------------------------------------------------------------ scheduler
         // Everything this grid reads from global memory is read after this point (the other warps only follow the
         // slots published below), so the grid may start while the worklist builder is still running.
@@ -268,7 +322,6 @@ __global__ void __launch_bounds__((NCW + 2) * 32, kDecodeCtasPerSm) decode_kerne
             }
             const bool bad = b < 0 || b >= p.B || h < 0 || h >= Hkv || s < 0 || pb < 0 || pe < pb;
             if (bad) {  // a task that is not from this plan: it writes a neutral state and takes no part in a merge
-                if (lane == 0) raise_status(ctx.status, PKV_STATUS_TASKS);
                 b = 0;
                 h = 0;
                 pb = pe = 0;
@@ -341,7 +394,7 @@ __global__ void __launch_bounds__((NCW + 2) * 32, kDecodeCtasPerSm) decode_kerne
                 atomicExch(&p.hdr->ctas_done, 0u);
             }
         }
-    } else if (warp == NCW) {
+    } else if (warp == NCW + 1) {
         // ------------------------------------------------------------------ loader
         if (lane == 0) {
             prefetch_tensormap(&p.tmap_k);
@@ -397,57 +450,136 @@ __global__ void __launch_bounds__((NCW + 2) * 32, kDecodeCtasPerSm) decode_kerne
         }
         // Wait for every copy this warp issued before the CTA may exit.
         for (int j = max(0, seq - NS); j < seq; ++j) warp_drain(&full[j % NS], (j / NS) & 1);
+    } else if (warp == NCW) {
+        // ------------------------------------------------------------------ epilogue
+        const bool fused = p.fuse_merge != 0 && p.variant != PKV_VARIANT_SINGLE;
+        float* mbuf = reinterpret_cast<float*>(smem + L::off_mbuf);
+        uint32_t missued = 0, mwaited = 0;
+        for (int tseq = 0;; ++tseq) {
+            const int e = tseq & 1;
+            if (!warp_wait(&efull[e], (tseq >> 1) & 1, ctx)) break;
+            const EpiHeader hd = ehdr[e];
+            if (hd.npages < 0) break;
+            const float* co = comb_o + e * L::kCombFloats;
+            const float2* cml = comb_ml + e * NCW * G;
+            for (int g = 0; g < G; ++g) {
+                float M = -INFINITY;
+#pragma unroll
+                for (int wi = 0; wi < NCW; ++wi) M = fmaxf(M, cml[wi * G + g].x);
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+                float lsum = 0.f;
+                if (M != -INFINITY) {
+#pragma unroll
+                    for (int wi = 0; wi < NCW; ++wi) {
+                        const float2 ml = cml[wi * G + g];
+                        const float f = fast_exp2(ml.x - M);
+                        lsum += f * ml.y;
+                        const float4 v = *reinterpret_cast<const float4*>(co + (wi * G + g) * kCombRow + lane * 4);
+                        a.x += f * v.x;
+                        a.y += f * v.y;
+                        a.z += f * v.z;
+                        a.w += f * v.w;
+                    }
+                }
+                if (p.variant == PKV_VARIANT_SINGLE) {
+                    store_half4(static_cast<__half*>(p.out) + ((size_t)hd.b * Hq + hd.h * G + g) * kHeadDim + lane * 4,
+                                a, lsum > 0.f ? 1.f / lsum : 0.f);
+                } else {
+                    const size_t state = (size_t)hd.task * G + g;
+                    if (lane == 0)
+                        reinterpret_cast<float2*>(p.ml)[state] =
+                            make_float2(M == -INFINITY ? -INFINITY : M * kLn2, lsum);
+                    reinterpret_cast<float4*>(p.acc + state * kHeadDim)[lane] = a;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&eempty[e]);  // the consumers may refill the slot
+            if (fused) {
+                // count the task in (b, h); the last arriver merges all S_b states of the pair
+                fence_acq_rel_gpu();  // this lane's state stores are performed before the arrival
+                __syncwarp();
+                int last = 0;
+                if (lane == 0 && hd.nsplit > 0) {
+                    uint32_t* cnt = p.counters + (size_t)hd.b * Hkv + hd.h;
+                    const uint32_t old = atomicAdd(cnt, 1u);
+                    last = old + 1u == (uint32_t)hd.nsplit;
+                    if (last) atomicExch(cnt, 0u);  // re-armed for the next step
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    fence_acq_rel_gpu();         // the other tasks' states, published before their arrivals ...
+                    fence_proxy_async_global();  // ... are visible to the bulk copies that read them
+                    if (!merge_pair<G, L::kMergeBufs>(p, hd.task - hd.s, hd.nsplit,
+                                       static_cast<__half*>(p.out) + ((size_t)hd.b * Hq + (size_t)hd.h * G) * kHeadDim,
+                                       mbuf, mbar, missued, mwaited, ctx, lane))
+                        break;
+                }
+            }
+        }
+        // Wait for the merge chunks still in flight (only after an abort can one be pending).
+        for (uint32_t j = mwaited; j < missued; ++j) warp_drain(&mbar[j % L::kMergeBufs], (j / L::kMergeBufs) & 1u);
     } else {
         // ------------------------------------------------------------------ consumers
         const int w = warp;
-        const int g0 = lane >> 2;        // query head (row of the mma tile) this lane holds
-        const int tq4 = 2 * (lane & 3);  // first token column this lane holds in each 8-token half
+        const int g8 = lane >> 2;  // groupID: token row of S^T / dim row of O^T; head column of the B operand
+        const int t4 = lane & 3;   // thread in group: head columns 2*t4, 2*t4 + 1 of S^T and O^T
         const int mi = lane >> 3, mr = lane & 7;
-        // ldmatrix row addresses: K (non-transposed) rows = tokens (mi >> 1) * 8 + mr, chunk parity mi & 1;
-        // V (transposed) rows = tokens (mi & 1) * 8 + mr, chunk parity mi >> 1.
-        const int k_row = ((mi >> 1) << 3) + mr, k_par = mi & 1;
-        const int v_row = ((mi & 1) << 3) + mr, v_par = mi >> 1;
+        // ldmatrix row addresses. K as the A operand (rows = tokens): matrix mi holds tokens (mi & 1) * 8 + mr at
+        // 16-byte chunk parity mi >> 1. V^T as the A operand via .trans (rows = dims): matrix mi holds tokens
+        // (mi >> 1) * 8 + mr at chunk parity mi & 1.
+        const int k_row = ((mi & 1) << 3) + mr, k_par = mi >> 1;
+        const int v_row = ((mi >> 1) << 3) + mr, v_par = mi & 1;
+        // P^T in the B-operand layout: lane (g, t) needs P[token 2t (+1, +8, +9)][head g], which lanes
+        // (2t) * 4 + g / 2 and (2t + 1) * 4 + g / 2 hold in the half g % 2 of their packed pairs.
+        const int src_a = (2 * t4) * 4 + (g8 >> 1), src_b = (2 * t4 + 1) * 4 + (g8 >> 1);
+        const uint32_t sel = (g8 & 1) ? 0x7632u : 0x5410u;
         const uint32_t stage0 = smem_addr(smem + L::off_stage);
-        float* comb_o = reinterpret_cast<float*>(smem + L::off_comb);
-        float2* comb_ml = reinterpret_cast<float2*>(smem + L::off_comb_ml);
         const float sl2 = p.scale_log2;
-        const bool fused = p.fuse_merge != 0 && p.variant != PKV_VARIANT_SINGLE;
         int seq = 0;
         for (int tseq = 0;; ++tseq) {
             const int ts = tseq % NTS;
+            const int e = tseq & 1;
             if (!warp_wait(&tmeta[ts], (tseq / NTS) & 1, ctx)) break;
             const int npages = slots[ts].npages;
-            if (npages < 0) break;
+            if (npages < 0) {  // no more tasks: tell the epilogue warp
+                if (!warp_wait(&eempty[e], ((tseq >> 1) & 1) ^ 1, ctx)) break;
+                if (w == 0 && lane == 0) ehdr[e].npages = -1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&efull[e]);
+                break;
+            }
             const int sb = slots[ts].b, sh = slots[ts].h, ss = slots[ts].s, stask = slots[ts].task;
             const int spb = slots[ts].page_begin, slen = slots[ts].seq_len, snsplit = slots[ts].nsplit;
             if (!warp_wait(&tq[ts], (tseq / NTS) & 1, ctx)) break;
-            // Query fragments (A operand rows = query heads of the group; rows >= G are zero).
-            uint32_t qa[8][4];
+            // Q^T as the B operand: b0 = Q[head][16ks + 2t, +1], b1 = Q[head][16ks + 2t + 8, +9], head = 8nt + g
+            uint32_t qb[8][kNT][2];
             {
                 const uint8_t* qs = smem + L::off_q + ts * L::kQRowsBytes;
-                const bool lo = g0 < G && npages > 0;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const int col = (ks * 16 + tq4) * 2;
-                    qa[ks][0] = lo ? *reinterpret_cast<const uint32_t*>(qs + g0 * kRowBytes + col) : 0u;
-                    qa[ks][2] = lo ? *reinterpret_cast<const uint32_t*>(qs + g0 * kRowBytes + col + 16) : 0u;
-                    if constexpr (G > 8) {
-                        const bool hi = g0 + 8 < G && npages > 0;
-                        qa[ks][1] = hi ? *reinterpret_cast<const uint32_t*>(qs + (g0 + 8) * kRowBytes + col) : 0u;
-                        qa[ks][3] = hi ? *reinterpret_cast<const uint32_t*>(qs + (g0 + 8) * kRowBytes + col + 16) : 0u;
-                    } else {
-                        qa[ks][1] = 0u;
-                        qa[ks][3] = 0u;
+                for (int nt = 0; nt < kNT; ++nt) {
+                    const int head = nt * 8 + g8;
+                    const bool on = head < G && npages > 0;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const int col = (ks * 16 + 2 * t4) * 2;
+                        qb[ks][nt][0] = on ? *reinterpret_cast<const uint32_t*>(qs + head * kRowBytes + col) : 0u;
+                        qb[ks][nt][1] = on ? *reinterpret_cast<const uint32_t*>(qs + head * kRowBytes + col + 16) : 0u;
                     }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[ts]);
 
-            float o[16][4];
+            // O^T accumulators: tile d of 16 dims; c0/c1 = dims 16d + g, heads 2t/2t+1; c2/c3 = dims 16d + g + 8
+            float o[kNT][8][4];
+            float m_a[kNT], m_b[kNT], l_a[kNT], l_b[kNT];  // running max / partial sum of head columns 2t, 2t+1
 #pragma unroll
-            for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-            float m_lo = -INFINITY, l_lo = 0.f, m_hi = -INFINITY, l_hi = 0.f;
+            for (int nt = 0; nt < kNT; ++nt) {
+                m_a[nt] = m_b[nt] = -INFINITY;
+                l_a[nt] = l_b[nt] = 0.f;
+#pragma unroll
+                for (int d = 0; d < 8; ++d) o[nt][d][0] = o[nt][d][1] = o[nt][d][2] = o[nt][d][3] = 0.f;
+            }
             bool aborted = false;
 
             // Page j of the CTA's page sequence lives in stage j % NS and is consumed by warp j % NCW. With
@@ -467,81 +599,71 @@ __global__ void __launch_bounds__((NCW + 2) * 32, kDecodeCtasPerSm) decode_kerne
                     // there. Their scores are masked below; their V rows are zeroed so 0 * (non-finite) cannot
                     // reach the accumulator.
                     uint8_t* vbase = smem + L::off_stage + st * kStageBytes + 2 * kBoxBytes;
-                    for (int e = lane; e < 2 * kPageSize * 8; e += 32) {
-                        const int box = e >> 7, r = (e >> 3) & 15, c = e & 7;
+                    for (int e2 = lane; e2 < 2 * kPageSize * 8; e2 += 32) {
+                        const int box = e2 >> 7, r = (e2 >> 3) & 15, c = e2 & 7;
                         if (r >= nvalid)
                             *reinterpret_cast<int4*>(vbase + box * kBoxBytes + r * 128 + c * 16) = make_int4(0, 0, 0, 0);
                     }
                     __syncwarp();
                 }
-                // S = Q K^T: two n8 tiles (tokens 0-7 and 8-15), k = head_dim in 8 steps of 16 columns
-                float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+                // S^T = K Q^T: rows = the 16 tokens, columns = 8 heads per tile, k = head_dim in 8 steps of 16
+                float sc[kNT][4];
+#pragma unroll
+                for (int nt = 0; nt < kNT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    uint32_t b0, b1, b2, b3;
+                    uint32_t a0, a1, a2, a3;
                     const uint32_t box = sbase + (ks >> 2) * kBoxBytes;
-                    ldsm_x4(box + swz(k_row, ((ks & 3) << 1) | k_par), b0, b1, b2, b3);
-                    mma_16816(s0, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-                    mma_16816(s1, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+                    ldsm_x4(box + swz(k_row, ((ks & 3) << 1) | k_par), a0, a1, a2, a3);
+#pragma unroll
+                    for (int nt = 0; nt < kNT; ++nt) mma_16816(sc[nt], a0, a1, a2, a3, qb[ks][nt][0], qb[ks][nt][1]);
                 }
-                // online softmax (base 2), row g0 and (G > 8) row g0 + 8
-                float x[4] = {s0[0] * sl2, s0[1] * sl2, s1[0] * sl2, s1[1] * sl2};
-                if (tq4 >= nvalid) x[0] = -INFINITY;
-                if (tq4 + 1 >= nvalid) x[1] = -INFINITY;
-                if (tq4 + 8 >= nvalid) x[2] = -INFINITY;
-                if (tq4 + 9 >= nvalid) x[3] = -INFINITY;
-                float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float mn = fmaxf(m_lo, mx);
-                const float mu = mn == -INFINITY ? 0.f : mn;
-                const float alpha = fast_exp2(m_lo - mu);
-                float pr[4];
+                uint32_t pb0[kNT], pb1[kNT];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) pr[e] = fast_exp2(x[e] - mu);
-                l_lo = l_lo * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
-                m_lo = mn;
-                const uint32_t pa0 = pack_half2(pr[0], pr[1]);
-                const uint32_t pa2 = pack_half2(pr[2], pr[3]);
-                uint32_t pa1 = 0u, pa3 = 0u;
-                float alpha_hi = 1.f;
-                if constexpr (G > 8) {
-                    float y[4] = {s0[2] * sl2, s0[3] * sl2, s1[2] * sl2, s1[3] * sl2};
-                    if (tq4 >= nvalid) y[0] = -INFINITY;
-                    if (tq4 + 1 >= nvalid) y[1] = -INFINITY;
-                    if (tq4 + 8 >= nvalid) y[2] = -INFINITY;
-                    if (tq4 + 9 >= nvalid) y[3] = -INFINITY;
-                    float my = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
-                    my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 1));
-                    my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 2));
-                    const float mnh = fmaxf(m_hi, my);
-                    const float muh = mnh == -INFINITY ? 0.f : mnh;
-                    alpha_hi = fast_exp2(m_hi - muh);
-                    float ph[4];
+                for (int nt = 0; nt < kNT; ++nt) {
+                    // online softmax (base 2) per head column: this lane holds tokens g and g + 8 of heads 2t, 2t+1
+                    float x0 = sc[nt][0] * sl2, x1 = sc[nt][1] * sl2, x2 = sc[nt][2] * sl2, x3 = sc[nt][3] * sl2;
+                    if (g8 >= nvalid) x0 = x1 = -INFINITY;
+                    if (g8 + 8 >= nvalid) x2 = x3 = -INFINITY;
+                    float ma = fmaxf(x0, x2), mb = fmaxf(x1, x3);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) ph[e] = fast_exp2(y[e] - muh);
-                    l_hi = l_hi * alpha_hi + ((ph[0] + ph[1]) + (ph[2] + ph[3]));
-                    m_hi = mnh;
-                    pa1 = pack_half2(ph[0], ph[1]);
-                    pa3 = pack_half2(ph[2], ph[3]);
-                }
-#pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    o[n][0] *= alpha;
-                    o[n][1] *= alpha;
-                    if constexpr (G > 8) {
-                        o[n][2] *= alpha_hi;
-                        o[n][3] *= alpha_hi;
+                    for (int off = 4; off < 32; off <<= 1) {
+                        ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, off));
+                        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
                     }
-                }
-                // O += P V: 16 n8 tiles over head_dim, k = the 16 tokens
+                    const float na = fmaxf(m_a[nt], ma), nb = fmaxf(m_b[nt], mb);
+                    const float ua = na == -INFINITY ? 0.f : na, ub = nb == -INFINITY ? 0.f : nb;
+                    const float alpha_a = fast_exp2(m_a[nt] - ua), alpha_b = fast_exp2(m_b[nt] - ub);
+                    const float p0 = fast_exp2(x0 - ua), p2 = fast_exp2(x2 - ua);
+                    const float p1 = fast_exp2(x1 - ub), p3 = fast_exp2(x3 - ub);
+                    l_a[nt] = l_a[nt] * alpha_a + (p0 + p2);
+                    l_b[nt] = l_b[nt] * alpha_b + (p1 + p3);
+                    m_a[nt] = na;
+                    m_b[nt] = nb;
 #pragma unroll
-                for (int n2 = 0; n2 < 8; ++n2) {
-                    uint32_t b0, b1, b2, b3;
-                    const uint32_t box = sbase + (2 + (n2 >> 2)) * kBoxBytes;
-                    ldsm_x4_trans(box + swz(v_row, ((n2 & 3) << 1) | v_par), b0, b1, b2, b3);
-                    mma_16816(o[2 * n2], pa0, pa1, pa2, pa3, b0, b1);
-                    mma_16816(o[2 * n2 + 1], pa0, pa1, pa2, pa3, b2, b3);
+                    for (int d = 0; d < 8; ++d) {
+                        o[nt][d][0] *= alpha_a;
+                        o[nt][d][1] *= alpha_b;
+                        o[nt][d][2] *= alpha_a;
+                        o[nt][d][3] *= alpha_b;
+                    }
+                    // P^T in the B-operand layout (tokens 2t, 2t+1 | 2t+8, 2t+9 of head g)
+                    const uint32_t h01 = pack_half2(p0, p1), h23 = pack_half2(p2, p3);
+                    const uint32_t va = __shfl_sync(0xffffffffu, h01, src_a);
+                    const uint32_t vb = __shfl_sync(0xffffffffu, h01, src_b);
+                    const uint32_t vc = __shfl_sync(0xffffffffu, h23, src_a);
+                    const uint32_t vd = __shfl_sync(0xffffffffu, h23, src_b);
+                    pb0[nt] = __byte_perm(va, vb, sel);
+                    pb1[nt] = __byte_perm(vc, vd, sel);
+                }
+                // O^T += V^T P^T: rows = 16 dims per tile (8 tiles), columns = heads, k = the 16 tokens
+#pragma unroll
+                for (int d = 0; d < 8; ++d) {
+                    uint32_t a0, a1, a2, a3;
+                    const uint32_t box = sbase + (2 + (d >> 2)) * kBoxBytes;
+                    ldsm_x4_trans(box + swz(v_row, ((d & 3) << 1) | v_par), a0, a1, a2, a3);
+#pragma unroll
+                    for (int nt = 0; nt < kNT; ++nt) mma_16816(o[nt][d], a0, a1, a2, a3, pb0[nt], pb1[nt]);
                 }
                 if (nvalid < kPageSize) fence_proxy_async_smem();  // zero stores before the next TMA write
                 __syncwarp();
@@ -550,103 +672,51 @@ __global__ void __launch_bounds__((NCW + 2) * 32, kDecodeCtasPerSm) decode_kerne
             if (aborted) break;
             seq += npages;
 
-            // ---- combine the NCW warps' states of this task
-            l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-            l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-            if constexpr (G > 8) {
-                l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-                l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-            }
-            if (!warp_wait(cempty, (tseq & 1) ^ 1, ctx)) break;
-            float* my_o = comb_o + w * G * kCombRow;
-            if (g0 < G) {
+            // ---- hand this warp's partial (m, l, O) of the task to the epilogue warp
 #pragma unroll
-                for (int n = 0; n < 16; ++n)
-                    *reinterpret_cast<float2*>(my_o + g0 * kCombRow + n * 8 + tq4) = make_float2(o[n][0], o[n][1]);
-                if ((lane & 3) == 0) comb_ml[w * G + g0] = make_float2(m_lo, l_lo);
-            }
-            if constexpr (G > 8) {
-                if (g0 + 8 < G) {
+            for (int nt = 0; nt < kNT; ++nt) {
 #pragma unroll
-                    for (int n = 0; n < 16; ++n)
-                        *reinterpret_cast<float2*>(my_o + (g0 + 8) * kCombRow + n * 8 + tq4) =
-                            make_float2(o[n][2], o[n][3]);
-                    if ((lane & 3) == 0) comb_ml[w * G + g0 + 8] = make_float2(m_hi, l_hi);
+                for (int off = 4; off < 32; off <<= 1) {
+                    l_a[nt] += __shfl_xor_sync(0xffffffffu, l_a[nt], off);
+                    l_b[nt] += __shfl_xor_sync(0xffffffffu, l_b[nt], off);
                 }
+            }
+            if (!warp_wait(&eempty[e], ((tseq >> 1) & 1) ^ 1, ctx)) break;
+            float* co = comb_o + e * L::kCombFloats + w * G * kCombRow;
+            float2* cml = comb_ml + e * NCW * G + w * G;
+#pragma unroll
+            for (int nt = 0; nt < kNT; ++nt) {
+                const int ha = nt * 8 + 2 * t4, hb = ha + 1;
+                if (ha < G) {
+#pragma unroll
+                    for (int d = 0; d < 8; ++d) {
+                        co[ha * kCombRow + d * 16 + g8] = o[nt][d][0];
+                        co[ha * kCombRow + d * 16 + g8 + 8] = o[nt][d][2];
+                    }
+                    if (g8 == 0) cml[ha] = make_float2(m_a[nt], l_a[nt]);
+                }
+                if (hb < G) {
+#pragma unroll
+                    for (int d = 0; d < 8; ++d) {
+                        co[hb * kCombRow + d * 16 + g8] = o[nt][d][1];
+                        co[hb * kCombRow + d * 16 + g8 + 8] = o[nt][d][3];
+                    }
+                    if (g8 == 0) cml[hb] = make_float2(m_b[nt], l_b[nt]);
+                }
+            }
+            if (w == 0 && lane == 0) {
+                EpiHeader hd;
+                hd.b = sb;
+                hd.h = sh;
+                hd.s = ss;
+                hd.task = stask;
+                hd.nsplit = snsplit;
+                hd.npages = npages;
+                hd.pad0 = hd.pad1 = 0;
+                ehdr[e] = hd;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(cfull);
-            if (!warp_wait(cfull, tseq & 1, ctx)) break;
-            for (int g = w; g < G; g += NCW) {
-                float M = -INFINITY;
-#pragma unroll
-                for (int wi = 0; wi < NCW; ++wi) M = fmaxf(M, comb_ml[wi * G + g].x);
-                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-                float lsum = 0.f;
-                if (M != -INFINITY) {
-#pragma unroll
-                    for (int wi = 0; wi < NCW; ++wi) {
-                        const float2 ml = comb_ml[wi * G + g];
-                        const float f = fast_exp2(ml.x - M);
-                        lsum += f * ml.y;
-                        const float4 v = *reinterpret_cast<const float4*>(comb_o + (wi * G + g) * kCombRow + lane * 4);
-                        a.x += f * v.x;
-                        a.y += f * v.y;
-                        a.z += f * v.z;
-                        a.w += f * v.w;
-                    }
-                }
-                const int hq = sh * G + g;
-                if (p.variant == PKV_VARIANT_SINGLE) {
-                    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-                    uint2 pk;
-                    pk.x = pack_half2(a.x * inv, a.y * inv);
-                    pk.y = pack_half2(a.z * inv, a.w * inv);
-                    __half* out = static_cast<__half*>(p.out) + ((size_t)sb * Hq + hq) * kHeadDim;
-                    *reinterpret_cast<uint2*>(out + lane * 4) = pk;
-                } else {
-                    const size_t state = (size_t)stask * G + g;
-                    if (lane == 0)
-                        reinterpret_cast<float2*>(p.ml)[state] =
-                            make_float2(M == -INFINITY ? -INFINITY : M * kLn2, lsum);
-                    reinterpret_cast<float4*>(p.acc + state * kHeadDim)[lane] = a;
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(cempty);
-
-            if (fused) {
-                // ---- fused merge: count this task in (b, h); the last arriver merges all S_b states. Two bounded
-                // barrier rounds: every warp's states are stored (and fenced) before warp 0 counts the task; the
-                // count's outcome is then broadcast. Phase k of either barrier completes before any warp can arrive
-                // for task k + 1, so the parities never alias.
-                __threadfence();  // this thread's state stores are visible device-wide before the arrival
-                __syncwarp();
-                if (lane == 0) mbar_arrive(mstate);
-                if (w == 0) {
-                    if (!warp_wait(mstate, tseq & 1, ctx)) break;
-                    if (lane == 0) {
-                        int last = 0;
-                        if (snsplit > 0) {
-                            uint32_t* cnt = p.counters + (size_t)sb * Hkv + sh;
-                            __threadfence();
-                            const uint32_t old = atomicAdd(cnt, 1u);
-                            last = old + 1u == (uint32_t)snsplit;
-                            if (last) atomicExch(cnt, 0u);  // re-armed for the next step
-                        }
-                        *last_flag = last;
-                        mbar_arrive(mlast);
-                    }
-                    __syncwarp();
-                }
-                if (!warp_wait(mlast, tseq & 1, ctx)) break;
-                if (*last_flag) {
-                    __threadfence();  // the other tasks' states, published before their arrivals, are read after
-                    for (int g = w; g < G; g += NCW)
-                        merge_group<G>(p, stask - ss, snsplit, g, lane,
-                                       static_cast<__half*>(p.out) + ((size_t)sb * Hq + (size_t)sh * G + g) * kHeadDim);
-                }
-            }
+            if (lane == 0) mbar_arrive(&efull[e]);
         }
     }
 }
@@ -675,7 +745,7 @@ int launch_g(const DecodeParams& p, int grid, bool pdl, cudaStream_t stream) {
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3((kNCW + 2) * 32);
+    cfg.blockDim = dim3((kNCW + 3) * 32);
     cfg.dynamicSmemBytes = L::total;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
