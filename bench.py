@@ -298,8 +298,11 @@ def time_workload(pkv, torch, wl, K, W, args, sms, dev, flush, stream):
     ev = timed_pass(True)
     status = pkv.pkv_read_status(ws)
     dec_ms = np.array([e[1].elapsed_time(e[2]) for e in ev])
+    merge_ms = np.array([e[2].elapsed_time(e[3]) for e in ev])  # zero-length pair unless the merge is separate
+    build_ms = np.array([e[0].elapsed_time(e[1]) for e in ev])
     kv_bytes = np.array([plans[j].kv_bytes for j in idx])
-    return {"idx": idx, "plans": [plans[j] for j in idx], "step_ms": step_ms, "dec_ms": dec_ms,
+    return {"idx": idx, "plans": [plans[j] for j in idx], "step_ms": step_ms, "dec_ms": dec_ms, "merge_ms": merge_ms,
+            "build_ms": build_ms,
             "kv_bytes": kv_bytes, "launches": launches, "status": status, "ws": ws, "out": out}
 
 
@@ -320,6 +323,7 @@ def summarize(pkv, wl, r, peak):
     tok = K * wl.B
     return {"by_tokens": by_tokens(wl, r),"tokens_per_s": tok / (r["step_ms"].sum() * 1e-3), "step_us_mean": 1e3 * float(r["step_ms"].mean()),
             "decode_us_mean": 1e3 * float(r["dec_ms"].mean()),
+            "merge_us_mean": 1e3 * float(r["merge_ms"].mean()), "build_us_mean": 1e3 * float(r["build_ms"].mean()),
             "decode_frac": float(r["kv_bytes"].sum() / (r["dec_ms"].sum() * 1e-3)) / 1e9 / peak,
             "step_frac": float(r["kv_bytes"].sum() / (r["step_ms"].sum() * 1e-3)) / 1e9 / peak,
             "algorithmic_bytes_per_step": float(r["kv_bytes"].mean()),
@@ -565,6 +569,7 @@ def run_ours(args):
                      "peak_source": f"hbm_gbs ({peak_kind})",
                      "algorithmic_bytes_per_launch": head["algorithmic_bytes_per_step"]},
         "decode_us_mean": head["decode_us_mean"], "step_us_mean": head["step_us_mean"],
+        "merge_us_mean": head["merge_us_mean"], "build_us_mean": head["build_us_mean"],
         "step_frac": head["step_frac"], "launches_per_step": head["launches_per_step"], "by_tokens": head["by_tokens"],
         "wall_us_per_step": wall_us, "wall_tokens_per_s": None if wall_us is None else B / (wall_us * 1e-6),
         "timed_wall_s": timed_wall, "gpu_launches": r["launches"], "device_status": int(r["status"]),

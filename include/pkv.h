@@ -65,6 +65,7 @@ extern "C" {
                                      row range in the workspace did not belong to the plan (it was skipped) */
 
 #define PKV_MAX_BATCH 4096
+#define PKV_MAX_ROWS_IN_DECODE 256 /* largest B for which the decode kernel can derive the workqueue itself */
 
 /* schedules */
 #define PKV_VARIANT_SINGLE 0    /* one task per (row, KV head), output normalised in the decode kernel */
@@ -81,18 +82,39 @@ typedef struct pkv_problem {
     int32_t max_pages_per_seq; /* columns of block_table */
 } pkv_problem;
 
-/* Constants of the roofline cost model used by pkv_plan (microseconds and GB/s). */
+/*
+ * Constants of the roofline cost model pkv_plan minimises (microseconds and GB/s; the v2 abstract's "calibrated
+ * roofline-style policy", the gist.science technical summary's "Calibrated Adaptive Policy"). For a candidate plan
+ * with T tasks on W resident CTAs, A = min(T, W) of them busy, kv = the step's K/V bytes and task bytes = c pages of
+ * one KV head's K and V:
+ *   workqueue (dynamic):   decode = launch_us + kv / min(hbm_gbs, A * wq_cta_gbs) + (T / W) * task_us
+ *                                   + tail * task_bytes / wq_cta_gbs
+ *   split, single (static): decode = launch_us + ceil(T / W) * (task_us + (kv / T) / min(cta_gbs, hbm_gbs / A))
+ *   merge  = merge_us + merge_state_us * S_max              separate merge kernel (launched with PDL)
+ *          | fused_us + fused_state_us * S_max * G          merge fused into the last task of each (row, KV head)
+ *   build  = build_us                                       workqueue with a builder launch
+ *   step   = decode + merge + build
+ * The rectangular split grid is a candidate only for B <= split_max_batch. pkv_policy_default returns the constants
+ * fitted by serving_paged_gqa_gb300/calibrate.py on the calibration traces (seeds 0-4); its held-out evaluation
+ * (seeds 5-9) is committed beside it.
+ */
 typedef struct pkv_policy {
-    double launch_us;      /* cost of one kernel launch in a step, including the gap to the previous kernel */
-    double hbm_gbs;        /* sustained KV streaming bandwidth of the decode kernel */
-    double cta_gbs;        /* streaming bandwidth one CTA reaches on its own (bounds a long task) */
-    double task_us;        /* fixed cost per task on one CTA (claim, q load, pipeline fill, state write) */
-    double merge_us;       /* fixed cost of the merge kernel beyond its launch */
-    double build_us;       /* fixed cost of the worklist builder beyond its launch */
-    double state_gbs;      /* bandwidth for writing + reading partial states */
-    int32_t ctas_per_sm;   /* resident decode CTAs per SM */
-    int32_t max_splits;    /* largest split count per row the policy may choose */
-    int32_t allow_variants;/* bit mask of PKV_VARIANT_* (1 << v) the policy may choose */
+    double launch_us;       /* decode launch, first bytes and teardown */
+    double hbm_gbs;         /* KV streaming bandwidth of the whole GPU */
+    double cta_gbs;         /* KV streaming bandwidth of one CTA of the static grid (split, single) */
+    double wq_cta_gbs;      /* KV streaming bandwidth of one CTA pulling from the workqueue */
+    double task_us;         /* per-task cost on one CTA (scheduling, q, epilogue) */
+    double tail;            /* workqueue: share of one task's time left over after the queue drains */
+    double merge_us;        /* separate merge: cost it adds to the step */
+    double merge_state_us;  /* separate merge: per split of the longest (row, KV head) */
+    double fused_us;        /* fused merge: cost of the last arrival and its merge */
+    double fused_state_us;  /* fused merge: per partial state one last arriver merges */
+    double build_us;        /* worklist builder launch (workqueue without the in-decode list) */
+    int32_t ctas_per_sm;    /* resident decode CTAs per SM (clamped to what fits) */
+    int32_t max_splits;     /* largest split count per row the policy may choose */
+    int32_t allow_variants; /* bit mask of PKV_VARIANT_* (1 << v) the policy may choose */
+    int32_t allow_fused;    /* 1: the policy may choose the fused merge */
+    int32_t split_max_batch;/* largest B for which the split grid is a candidate */
     int32_t reserved;
 } pkv_policy;
 
@@ -108,6 +130,12 @@ typedef struct pkv_plan_t {
                             (row, KV head) to finish merges them and writes out; pkv_merge is then a no-op);
                             0 = pkv_decode writes partial states only and pkv_merge combines them. The planners set
                             1; a caller may set 0 (the workspace layout does not depend on it). */
+    int32_t list_in_decode; /* workqueue: 1 = the decode kernel derives the compact list itself from seq_lens (every
+                               CTA scans the per-row split counts into shared memory; CTA 0 publishes row_off /
+                               row_splits / task_count), so no pkv_build_worklist launch is needed; 0 = the decode
+                               runs the list pkv_build_worklist wrote. The planners set 1 when B <= PKV_MAX_ROWS_IN_DECODE.
+                               Both give the same task order (b, h_kv, s). */
+    int32_t reserved;
     pkv_problem problem; /* copy of the problem the plan was made for; later calls must pass an equal one */
     int64_t task_capacity;  /* task slots reserved in the workspace */
     int64_t state_capacity; /* partial-state slots reserved in the workspace */
@@ -149,7 +177,7 @@ const char* pkv_strerror(int code);
 /* Validates a problem against the supported set. Host only. */
 int pkv_check_problem(const pkv_problem* problem);
 
-/* Fills *policy with the built-in cost-model constants. */
+/* Fills *policy with the built-in cost-model constants (fitted on the calibration traces, seeds 0-4). */
 void pkv_policy_default(pkv_policy* policy);
 
 /*
@@ -162,7 +190,8 @@ int pkv_plan(const pkv_problem* problem, const int32_t* seq_lens_host, int32_t n
              pkv_plan_t* plan);
 
 /* Same as pkv_plan with the schedule and split size fixed by the caller (chunk_pages >= 1; ignored for
- * PKV_VARIANT_SINGLE). ctas_per_sm <= 0 means the default. Used by tests and calibration sweeps. */
+ * PKV_VARIANT_SINGLE). ctas_per_sm <= 0 means the default. The merge mode (fuse_merge) is the one the default
+ * policy predicts faster; the caller may change it. Used by tests and calibration sweeps. */
 int pkv_plan_fixed(const pkv_problem* problem, const int32_t* seq_lens_host, int32_t num_sms, int32_t variant,
                    int32_t chunk_pages, int32_t ctas_per_sm, pkv_plan_t* plan);
 
@@ -191,7 +220,8 @@ int pkv_build_worklist(const pkv_plan_t* plan, const pkv_problem* problem, const
  *   split / workqueue: one task per (row, KV head, split) writes the partial (m, l, acc) state of its G query heads
  *     into the workspace (empty rectangular splits write m = -inf, l = 0, acc = 0). With plan->fuse_merge = 1 the
  *     last task of each (row, KV head) also merges that pair's states and writes out; with 0, follow with pkv_merge.
- *   workqueue: runs the list the last pkv_build_worklist wrote into ws (call it first, on the same stream).
+ *   workqueue: with plan->list_in_decode = 0 runs the list the last pkv_build_worklist wrote into ws (call it first,
+ *     on the same stream); with 1 derives the same list from seq_lens_dev itself.
  * scale multiplies q.k (use 1/sqrt(head_dim)). out may be NULL only for split / workqueue plans with fuse_merge 0.
  * Rows longer than the plan's lengths (seq_lens grew after pkv_plan) raise PKV_STATUS_TASKS; their extra pages are
  * not read.
@@ -209,7 +239,8 @@ int pkv_decode(const pkv_plan_t* plan, const pkv_problem* problem, const void* q
 int pkv_merge(const pkv_plan_t* plan, const pkv_problem* problem, void* ws, size_t ws_bytes, void* out,
               void* stream);
 
-/* Convenience: build (workqueue) + decode + merge for one step on one stream. */
+/* Convenience: build (workqueue with list_in_decode = 0) + decode + merge (fuse_merge = 0) for one step on one
+ * stream. */
 int pkv_decode_step(const pkv_plan_t* plan, const pkv_problem* problem, const void* q, const void* k_pool,
                     const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev, float scale,
                     void* ws, size_t ws_bytes, void* out, void* stream);

@@ -26,6 +26,7 @@ PKV_STATUS_TIMEOUT = 0x4
 PKV_STATUS_TASKS = 0x8
 
 PKV_MAX_BATCH = 4096
+PKV_MAX_ROWS_IN_DECODE = 256
 
 PKV_VARIANT_SINGLE = 0
 PKV_VARIANT_SPLIT = 1
@@ -50,15 +51,21 @@ class Problem(ctypes.Structure):
 
 class Policy(ctypes.Structure):
     _fields_ = [("launch_us", ctypes.c_double), ("hbm_gbs", ctypes.c_double), ("cta_gbs", ctypes.c_double),
-                ("task_us", ctypes.c_double), ("merge_us", ctypes.c_double), ("build_us", ctypes.c_double),
-                ("state_gbs", ctypes.c_double), ("ctas_per_sm", ctypes.c_int32), ("max_splits", ctypes.c_int32),
-                ("allow_variants", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("wq_cta_gbs", ctypes.c_double), ("task_us", ctypes.c_double), ("tail", ctypes.c_double),
+                ("merge_us", ctypes.c_double), ("merge_state_us", ctypes.c_double), ("fused_us", ctypes.c_double),
+                ("fused_state_us", ctypes.c_double), ("build_us", ctypes.c_double), ("ctas_per_sm", ctypes.c_int32),
+                ("max_splits", ctypes.c_int32), ("allow_variants", ctypes.c_int32), ("allow_fused", ctypes.c_int32),
+                ("split_max_batch", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+    CONSTANTS = ("launch_us", "hbm_gbs", "cta_gbs", "wq_cta_gbs", "task_us", "tail", "merge_us", "merge_state_us",
+                 "fused_us", "fused_state_us", "build_us")
 
 
 class Plan(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int32), ("chunk_pages", ctypes.c_int32), ("num_splits", ctypes.c_int32),
                 ("num_tasks", ctypes.c_int32), ("grid_ctas", ctypes.c_int32), ("group", ctypes.c_int32),
-                ("num_sms", ctypes.c_int32), ("fuse_merge", ctypes.c_int32), ("problem", Problem),
+                ("num_sms", ctypes.c_int32), ("fuse_merge", ctypes.c_int32), ("list_in_decode", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("problem", Problem),
                 ("task_capacity", ctypes.c_int64), ("state_capacity", ctypes.c_int64),
                 ("ws_bytes", ctypes.c_int64), ("off_counters", ctypes.c_int64), ("off_row_off", ctypes.c_int64),
                 ("off_row_splits", ctypes.c_int64),
@@ -68,7 +75,8 @@ class Plan(ctypes.Structure):
     def describe(self) -> dict:
         return {"variant": VARIANT_NAMES.get(self.variant, self.variant), "chunk_pages": self.chunk_pages,
                 "num_splits": self.num_splits, "num_tasks": self.num_tasks, "grid_ctas": self.grid_ctas,
-                "fuse_merge": self.fuse_merge, "ws_bytes": self.ws_bytes, "predicted_us": self.predicted_us}
+                "fuse_merge": self.fuse_merge, "list_in_decode": self.list_in_decode, "ws_bytes": self.ws_bytes,
+                "predicted_us": self.predicted_us}
 
 
 _lib = None

@@ -23,8 +23,10 @@ int check_plan(const pkv_plan_t* plan, const pkv_problem* pr, const void* ws, si
     if (!same_problem(plan->problem, *pr)) return PKV_E_INVAL;
     if (plan->variant < PKV_VARIANT_SINGLE || plan->variant > PKV_VARIANT_WORKQUEUE) return PKV_E_INVAL;
     if (plan->group != pr->num_q_heads / pr->num_kv_heads || plan->grid_ctas <= 0 || plan->chunk_pages <= 0 ||
-        plan->num_splits <= 0 || plan->num_tasks < 0 || (plan->fuse_merge != 0 && plan->fuse_merge != 1))
+        plan->num_splits <= 0 || plan->num_tasks < 0 || (plan->fuse_merge != 0 && plan->fuse_merge != 1) ||
+        (plan->list_in_decode != 0 && plan->list_in_decode != 1))
         return PKV_E_INVAL;
+    if (plan->list_in_decode && pr->batch > PKV_MAX_ROWS_IN_DECODE) return PKV_E_UNSUPPORTED;
     if (plan->off_counters < (int64_t)sizeof(pkv_ws_header) ||
         plan->off_counters + 4 * (int64_t)pr->batch * pr->num_kv_heads > plan->ws_bytes)
         return PKV_E_INVAL;
@@ -172,7 +174,7 @@ int decode_step(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, co
                          cudaSuccess)
             return PKV_E_CUDA;
     }
-    if (plan->variant == PKV_VARIANT_WORKQUEUE) {
+    if (plan->variant == PKV_VARIANT_WORKQUEUE && !plan->list_in_decode) {
         rc = pkv_build_worklist(plan, pr, seq_lens_dev, ws, ws_bytes, stream);
         if (rc != PKV_OK) return rc;
     }
@@ -206,7 +208,8 @@ extern "C" int pkv_decode(const pkv_plan_t* plan, const pkv_problem* pr, const v
     p.ml = at<float>(ws, plan->off_ml);
     p.acc = at<float>(ws, plan->off_acc);
     p.tasks = at<const pkv_task>(ws, plan->off_tasks);
-    p.row_splits = at<const int32_t>(ws, plan->off_row_splits);
+    p.row_off = at<int32_t>(ws, plan->off_row_off);
+    p.row_splits = at<int32_t>(ws, plan->off_row_splits);
     p.counters = at<uint32_t>(ws, plan->off_counters);
     p.hdr = static_cast<pkv_ws_header*>(ws);
     p.B = pr->batch;
@@ -220,10 +223,11 @@ extern "C" int pkv_decode(const pkv_plan_t* plan, const pkv_problem* pr, const v
     p.num_tasks = plan->num_tasks;
     p.task_capacity = (int32_t)plan->task_capacity;
     p.fuse_merge = plan->variant != PKV_VARIANT_SINGLE && plan->fuse_merge;
+    p.list_in_decode = plan->variant == PKV_VARIANT_WORKQUEUE && plan->list_in_decode;
     p.scale_log2 = scale * 1.4426950408889634f;
     // The workqueue decode follows its builder: let it start while the builder runs (it reads the builder's output
     // only after griddepcontrol.wait).
-    const bool pdl = plan->variant == PKV_VARIANT_WORKQUEUE;
+    const bool pdl = plan->variant == PKV_VARIANT_WORKQUEUE && !plan->list_in_decode;
     return cuda_rc(launch_decode(p, plan->group, plan->grid_ctas, pdl, stream));
 }
 

@@ -9,8 +9,8 @@
 // neutral states for empty splits ("Row-Local Bounds"), compact workqueue ("Compact Workqueue")).
 //
 // CTA layout (persistent over tasks; grid = one wave of resident CTAs):
-//   warp NCW+2  scheduler: takes tasks (split / single: a static stride over the task space, KV heads fastest, so the
-//               CTAs that start together read the same pages; workqueue: an atomic queue head over the built list,
+//   warp NCW+2  scheduler: takes tasks (split / single: a static stride over the (b, h, s) task space; workqueue: an
+//               atomic queue head over the built list in the same order,
 //               after waiting for the builder grid), fetches the row length and the task's first 32 block-table
 //               entries together, publishes both in a shared-memory task slot, then bulk-copies the G query rows of
 //               the task into the slot (completion on a separate barrier, so the loader never waits for q);
@@ -64,14 +64,15 @@ struct Layout {
     static constexpr int kNT = (G + 7) / 8;  // 8-head column tiles of the MMAs
     static constexpr int kQRowsBytes = ((G * kRowBytes + 127) / 128) * 128;
     static constexpr int kCombFloats = NCW * G * kCombRow;  // one slot: every consumer warp's O rows
-    static constexpr int kMergeBufs = G <= 4 ? 3 : 2;       // merge chunks in flight (what two CTAs' shared memory allows)
+    static constexpr int kMergeBufs = 2;                    // merge chunks in flight
     static constexpr int off_stage = 0;  // 1024-byte aligned (128-byte swizzle atom)
     static constexpr int off_q = off_stage + NS * kStageBytes;
     static constexpr int off_mbuf = off_q + NTS * kQRowsBytes;             // 2 merge chunks (bulk copy targets)
     static constexpr int off_comb = off_mbuf + kMergeBufs * kMergeChunk * kHeadDim * 4;
     static constexpr int off_comb_ml = off_comb + 2 * kCombFloats * 4;    // float2 (m, l) per slot/warp/head
     static constexpr int off_ehdr = off_comb_ml + 2 * NCW * G * 8;
-    static constexpr int off_slots = off_ehdr + 2 * (int)sizeof(EpiHeader);
+    static constexpr int off_rows = off_ehdr + 2 * (int)sizeof(EpiHeader);  // in-decode list: off, S_b, L_b per row
+    static constexpr int off_slots = off_rows + 3 * PKV_MAX_ROWS_IN_DECODE * 4;
     static constexpr int off_bars = ((off_slots + NTS * (int)sizeof(TaskSlot) + 15) / 16) * 16;
     static constexpr int nbars = 2 * NS + 3 * NTS + 4 + kMergeBufs;
     static constexpr int off_flag = off_bars + nbars * 8;
@@ -269,15 +270,58 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
         grid_dependency_wait();
         const int variant = p.variant;
         const bool wq = variant == PKV_VARIANT_WORKQUEUE;
+        const bool in_decode = wq && p.list_in_decode;
+        int* row_off_s = reinterpret_cast<int*>(smem + L::off_rows);
+        int* row_S_s = row_off_s + PKV_MAX_ROWS_IN_DECODE;
+        int* row_L_s = row_S_s + PKV_MAX_ROWS_IN_DECODE;
         int count = p.num_tasks;
-        if (wq) count = min(*reinterpret_cast<volatile int32_t*>(&p.hdr->task_count), p.task_capacity);
+        if (in_decode) {
+            // The compact list of the step, derived here: S_b = ceil(ceil(L_b / page_size) / c) and the exclusive
+            // scan of Hkv * S_b over the rows (the builder's arithmetic, "Compact Workqueue"). Task t of the list
+            // belongs to the last row b with off_b <= t.
+            int run = 0;
+            for (int b0 = 0; b0 < p.B; b0 += 32) {
+                const int b = b0 + lane;
+                int len = b < p.B ? p.seq_lens[b] : 0;
+                if (len < 0 || len > p.max_pages * kPageSize) {
+                    if (blockIdx.x == 0) raise_status(ctx.status, PKV_STATUS_BAD_LEN);
+                    len = 0;
+                }
+                const int S = ((len + kPageSize - 1) / kPageSize + p.chunk_pages - 1) / p.chunk_pages;
+                const int x = b < p.B ? Hkv * S : 0;
+                int incl = x;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                if (b < p.B) {
+                    row_off_s[b] = run + incl - x;
+                    row_S_s[b] = S;
+                    row_L_s[b] = len;
+                    if (blockIdx.x == 0) {  // published for the separate merge kernel (and for inspection)
+                        p.row_off[b] = run + incl - x;
+                        p.row_splits[b] = S;
+                    }
+                }
+                run += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            __syncwarp();
+            count = min(run, p.task_capacity);
+            if (blockIdx.x == 0 && lane == 0) {
+                p.hdr->task_count = count;
+                if (run > p.task_capacity) raise_status(ctx.status, PKV_STATUS_TASKS);
+            }
+        } else if (wq) {
+            count = min(*reinterpret_cast<volatile int32_t*>(&p.hdr->task_count), p.task_capacity);
+        }
         const __half* q = static_cast<const __half*>(p.q);
         int tseq = 0;
         for (int k = 0;; ++k) {
             int t;
-            if (wq) {
+            if (wq && k > 0) {  // the first wave is static: CTA i starts with task i, no atomic on its critical path
                 int c = 0;
-                if (lane == 0) c = static_cast<int>(atomicAdd(&p.hdr->queue_head, 1u));
+                if (lane == 0) c = static_cast<int>(gridDim.x + atomicAdd(&p.hdr->queue_head, 1u));
                 t = __shfl_sync(0xffffffffu, c, 0);
             } else {
                 t = blockIdx.x + k * gridDim.x;
@@ -293,7 +337,24 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
                 break;
             }
             int b, h, s, pb, pe, task, nsplit = 1;
-            if (wq) {
+            if (in_decode) {
+                int lo = 0, hi = p.B - 1;  // rows without tasks share their successor's offset and are skipped
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (row_off_s[mid] <= t)
+                        lo = mid;
+                    else
+                        hi = mid - 1;
+                }
+                b = lo;
+                const int Sb = max(row_S_s[b], 1);
+                const int r = t - row_off_s[b];
+                h = r / Sb;
+                s = r - h * Sb;
+                pb = s * p.chunk_pages;
+                pe = min(pb + p.chunk_pages, (row_L_s[b] + kPageSize - 1) / kPageSize);
+                task = t;
+            } else if (wq) {
                 const pkv_task tk = p.tasks[t];
                 b = tk.row;
                 h = tk.head_split >> 16;
@@ -302,15 +363,17 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
                 pe = tk.page_end;
                 task = t;
             } else if (variant == PKV_VARIANT_SPLIT) {
+                // (b, h, s) order, splits fastest: the CTAs that run at the same time read different page ranges of
+                // one head (measured faster on GB300 than eight CTAs reading the eight heads of the same pages)
                 const int S = p.num_splits;
                 const int per_row = Hkv * S;
                 b = t / per_row;
                 const int r = t - b * per_row;
-                s = r / Hkv;
-                h = r - s * Hkv;
+                h = r / S;
+                s = r - h * S;
                 pb = s * p.chunk_pages;
                 pe = pb + p.chunk_pages;
-                task = (b * Hkv + h) * S + s;
+                task = t;
                 nsplit = S;
             } else {
                 b = t / Hkv;
@@ -330,7 +393,7 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
             const int nent = max(0, min(min(pe, p.max_pages) - pb, kSlotEntries));
             const int ent = lane < nent ? p.block_table[(size_t)b * p.max_pages + pb + lane] : -1;
             int len = p.seq_lens[b];
-            const int row_splits = wq ? p.row_splits[b] : 0;
+            const int row_splits = in_decode ? row_S_s[b] : (wq ? p.row_splits[b] : 0);
             if (len < 0 || len > p.max_pages * kPageSize) {
                 if (lane == 0) raise_status(ctx.status, PKV_STATUS_BAD_LEN);
                 len = 0;

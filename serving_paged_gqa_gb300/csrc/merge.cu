@@ -6,13 +6,13 @@
 //   M = max_s m_s over states with l_s > 0,  out = sum_s e^(m_s - M) acc_s / sum_s e^(m_s - M) l_s.
 // Neutral states (empty splits: m = -inf, l = 0) contribute nothing; a row with none gets 0.
 //
-// One CTA of 4 warps per (b, hq). The states are split across the warps (warp w takes s = w, w + 4, ...); lane k
+// One CTA of 16 warps per (b, hq). The states are split across the warps (warp w takes s = w, w + 16, ...); lane k
 // owns dimensions 4k..4k+3, so one state is one coalesced 512-byte load per warp. The (m, l) pairs give M in one
 // block-wide pass, while the first round of acc loads is already in flight; then each warp accumulates its states
-// 8 at a time (all 8 loads issued before use), and the 4 partial sums meet in shared memory. A merge of S states
-// costs about 1 + S/32 L2 round trips. The grid is launched with programmatic stream serialization after the decode:
-// it may be scheduled while the decode runs (128 threads of at most 64 registers fit beside two decode CTAs) and
-// reads the states only after griddepcontrol.wait.
+// 8 at a time (all 8 loads issued before use), and the 16 partial sums meet in shared memory. With 128 states in
+// flight per CTA a merge of S states costs about 1 + S/128 memory round trips (the merge is latency-bound: its
+// states are a few MB). The grid is launched with programmatic stream serialization after the decode and reads the
+// states only after griddepcontrol.wait.
 #include <cuda_fp16.h>
 
 #include "pkv_internal.h"
@@ -21,7 +21,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = 16;
 constexpr int kRound = 8;  // states per warp whose loads are in flight together
 constexpr float kLog2e = 1.4426950408889634f;
 

@@ -32,12 +32,14 @@ struct DecodeParams {
     float* ml;             // float2 (m, l) per state
     float* acc;            // float [state][d]
     const pkv_task* tasks;      // workqueue only
-    const int32_t* row_splits;  // workqueue only: the builder's S_b per row
+    int32_t* row_off;           // workqueue only: the list's first task of each row (written here if list_in_decode)
+    int32_t* row_splits;        // workqueue only: S_b per row (the builder's, or written here if list_in_decode)
     uint32_t* counters;         // fused merge: arrivals per (row, KV head), zero between steps
     pkv_ws_header* hdr;
     int32_t B, Hq, Hkv, num_pages, max_pages;
     int32_t chunk_pages, num_splits, variant, num_tasks, task_capacity;
     int32_t fuse_merge;         // 1: the last task of each (row, KV head) merges its states and writes out
+    int32_t list_in_decode;     // workqueue: derive the compact list from seq_lens in every CTA
     float scale_log2;           // scale * log2(e): scores are kept in base-2 units inside the kernel
 };
 

@@ -5,19 +5,16 @@
 // routes each step to one execution path; the gist.science technical summary, "Calibrated Adaptive Policy", keys
 // that choice on batch size B and the longest context N_max. Here the candidates are this library's own
 // single-pass kernel, the rectangular split grid and the compact workqueue, each over a set of split sizes c
-// (pages per split), and the model predicts a step's time as
-//   launches * launch_us
-//   + max(KV bytes / hbm_gbs, sum_i cost_i / W, max_i cost_i)        (decode; W = resident CTAs, cost_i =
-//                                                                      task_us + bytes_i / cta_gbs per task)
-//   + merge_us + 2 * state bytes / state_gbs                          (split and workqueue)
-//   + build_us                                                         (workqueue)
-// and keeps the cheapest candidate.
+// (pages per split) and with the separate or the fused merge; the model (include/pkv.h, pkv_policy) predicts each
+// candidate's step time and the cheapest is kept. Its constants come from policy_constants.h, which the
+// calibration tool writes.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <vector>
 
 #include "pkv_internal.h"
+#include "policy_constants.h"
 
 namespace {
 
@@ -46,16 +43,22 @@ extern "C" int pkv_check_problem(const pkv_problem* pr) {
 extern "C" void pkv_policy_default(pkv_policy* pol) {
     if (!pol) return;
     std::memset(pol, 0, sizeof(*pol));
-    pol->launch_us = 2.5;
-    pol->hbm_gbs = 5500.0;
-    pol->cta_gbs = 40.0;
-    pol->task_us = 1.5;
-    pol->merge_us = 1.0;
-    pol->build_us = 1.0;
-    pol->state_gbs = 3000.0;
-    pol->ctas_per_sm = 2;
-    pol->max_splits = 256;
+    pol->launch_us = PKV_FIT_LAUNCH_US;
+    pol->hbm_gbs = PKV_FIT_HBM_GBS;
+    pol->cta_gbs = PKV_FIT_CTA_GBS;
+    pol->wq_cta_gbs = PKV_FIT_WQ_CTA_GBS;
+    pol->task_us = PKV_FIT_TASK_US;
+    pol->tail = PKV_FIT_TAIL;
+    pol->merge_us = PKV_FIT_MERGE_US;
+    pol->merge_state_us = PKV_FIT_MERGE_STATE_US;
+    pol->fused_us = PKV_FIT_FUSED_US;
+    pol->fused_state_us = PKV_FIT_FUSED_STATE_US;
+    pol->build_us = PKV_FIT_BUILD_US;
+    pol->ctas_per_sm = kDecodeCtasPerSm;
+    pol->max_splits = 1024;
     pol->allow_variants = (1 << PKV_VARIANT_SINGLE) | (1 << PKV_VARIANT_SPLIT) | (1 << PKV_VARIANT_WORKQUEUE);
+    pol->allow_fused = 1;
+    pol->split_max_batch = 2;
 }
 
 namespace {
@@ -107,6 +110,7 @@ int fill_plan(const pkv_problem* pr, const int32_t* lens, int32_t num_sms, int32
     plan->num_splits = (int32_t)splits;
     plan->num_tasks = (int32_t)tasks;
     plan->fuse_merge = variant == PKV_VARIANT_SINGLE ? 0 : 1;
+    plan->list_in_decode = variant == PKV_VARIANT_WORKQUEUE && B <= PKV_MAX_ROWS_IN_DECODE ? 1 : 0;
     plan->group = G;
     plan->num_sms = num_sms;
     plan->problem = *pr;
@@ -135,36 +139,59 @@ int fill_plan(const pkv_problem* pr, const int32_t* lens, int32_t num_sms, int32
     return PKV_OK;
 }
 
+// Step time of a plan under the model documented with pkv_policy (include/pkv.h).
 double predict_us(const pkv_policy* pol, const pkv_plan_t* plan, const int32_t* lens) {
     const pkv_problem& pr = plan->problem;
-    const int B = pr.batch, Hkv = pr.num_kv_heads, G = plan->group;
-    const int c = plan->chunk_pages;
+    const int B = pr.batch, G = plan->group;
+    const double T = plan->num_tasks;
+    if (T <= 0) return pol->launch_us;
     const double W = (double)std::max(1, plan->grid_ctas);
-    const double per_tok = (double)kTokenHeadBytes;  // K + V bytes of one token for one KV head
-    double sum_cost = 0.0, max_cost = 0.0;
-    for (int b = 0; b < B; ++b) {
-        const int64_t L = lens[b];
-        const int64_t P = (L + kPageSize - 1) / kPageSize;
-        const int64_t S = plan->variant == PKV_VARIANT_SINGLE ? 1 : (P + c - 1) / c;
-        int64_t S_grid = S;
-        if (plan->variant == PKV_VARIANT_SPLIT) S_grid = plan->num_splits;
-        for (int64_t s = 0; s < S_grid; ++s) {
-            int64_t t0 = s * c * kPageSize, t1 = std::min<int64_t>((s + 1) * (int64_t)c * kPageSize, L);
-            if (plan->variant == PKV_VARIANT_SINGLE) t0 = 0, t1 = L;
-            const double tok = t1 > t0 ? (double)(t1 - t0) : 0.0;
-            const double cost = pol->task_us + tok * per_tok / (pol->cta_gbs * 1e3);
-            sum_cost += cost * Hkv;
-            max_cost = std::max(max_cost, cost);
-        }
+    const double A = std::min(T, W);
+    int64_t p_max = 0;
+    for (int b = 0; b < B; ++b) p_max = std::max<int64_t>(p_max, ((int64_t)lens[b] + kPageSize - 1) / kPageSize);
+    const double pages_per_task = plan->variant == PKV_VARIANT_SINGLE ? (double)p_max
+                                                                       : (double)std::min<int64_t>(plan->chunk_pages, p_max);
+    const double task_bytes = pages_per_task * kPageSize * kTokenHeadBytes;
+    const double gb = 1e3;  // bytes / (GB/s * 1e3) = microseconds
+    double t;
+    if (plan->variant == PKV_VARIANT_WORKQUEUE) {
+        t = pol->launch_us + plan->kv_bytes / (std::min(pol->hbm_gbs, A * pol->wq_cta_gbs) * gb) +
+            (T / W) * pol->task_us + pol->tail * task_bytes / (pol->wq_cta_gbs * gb);
+    } else {
+        const double share = std::min(pol->cta_gbs, pol->hbm_gbs / A) * gb;
+        t = pol->launch_us + std::ceil(T / W) * (pol->task_us + (plan->kv_bytes / T) / share);
     }
-    const double stream_us = plan->kv_bytes / (pol->hbm_gbs * 1e3);
-    double t = pol->launch_us + std::max(stream_us, std::max(sum_cost / W, max_cost));
     if (plan->variant != PKV_VARIANT_SINGLE) {
-        const double states = (double)plan->num_tasks * G;
-        t += pol->launch_us + pol->merge_us + 2.0 * states * kStateBytes / (pol->state_gbs * 1e3);
+        const double s_max = plan->variant == PKV_VARIANT_SPLIT
+                                 ? (double)plan->num_splits
+                                 : std::ceil((double)p_max / std::max(1, plan->chunk_pages));
+        if (plan->fuse_merge)
+            t += pol->fused_us + pol->fused_state_us * s_max * G;
+        else
+            t += pol->merge_us + pol->merge_state_us * s_max;
     }
-    if (plan->variant == PKV_VARIANT_WORKQUEUE) t += pol->launch_us + pol->build_us;
+    if (plan->variant == PKV_VARIANT_WORKQUEUE && !plan->list_in_decode) t += pol->build_us;
     return t;
+}
+
+// Picks the cheaper merge mode for a split or workqueue plan (the fused one only if allowed).
+void choose_merge(const pkv_policy* pol, pkv_plan_t* plan, const int32_t* lens) {
+    if (plan->variant == PKV_VARIANT_SINGLE) {
+        plan->fuse_merge = 0;
+        plan->predicted_us = predict_us(pol, plan, lens);
+        return;
+    }
+    plan->fuse_merge = 0;
+    const double sep = predict_us(pol, plan, lens);
+    plan->predicted_us = sep;
+    if (pol->allow_fused) {
+        plan->fuse_merge = 1;
+        const double fused = predict_us(pol, plan, lens);
+        if (fused < sep)
+            plan->predicted_us = fused;
+        else
+            plan->fuse_merge = 0;
+    }
 }
 
 }  // namespace
@@ -175,8 +202,7 @@ extern "C" int pkv_plan_fixed(const pkv_problem* pr, const int32_t* lens, int32_
     if (rc != PKV_OK) return rc;
     pkv_policy pol;
     pkv_policy_default(&pol);
-    pol.ctas_per_sm = ctas_per_sm > 0 ? ctas_per_sm : pol.ctas_per_sm;
-    plan->predicted_us = predict_us(&pol, plan, lens);
+    choose_merge(&pol, plan, lens);
     return PKV_OK;
 }
 
@@ -190,8 +216,8 @@ extern "C" int pkv_plan(const pkv_problem* pr, const int32_t* lens, int32_t num_
         pol = *policy;
     else
         pkv_policy_default(&pol);
-    if (pol.ctas_per_sm <= 0 || pol.max_splits <= 0 || pol.hbm_gbs <= 0 || pol.cta_gbs <= 0 ||
-        pol.state_gbs <= 0)
+    if (pol.ctas_per_sm <= 0 || pol.max_splits <= 0 || !(pol.hbm_gbs > 0) || !(pol.cta_gbs > 0) ||
+        !(pol.wq_cta_gbs > 0))
         return PKV_E_INVAL;
     int64_t max_pages = 0;
     for (int b = 0; b < pr->batch; ++b) {
@@ -211,10 +237,11 @@ extern "C" int pkv_plan(const pkv_problem* pr, const int32_t* lens, int32_t num_
     pkv_plan_t best{}, cand{};
     for (int v = PKV_VARIANT_SINGLE; v <= PKV_VARIANT_WORKQUEUE; ++v) {
         if (!(pol.allow_variants & (1 << v))) continue;
+        if (v == PKV_VARIANT_SPLIT && pr->batch > pol.split_max_batch) continue;
         const size_t n = v == PKV_VARIANT_SINGLE ? 1 : chunks.size();
         for (size_t i = 0; i < n; ++i) {
             if (fill_plan(pr, lens, num_sms, v, chunks[i], pol.ctas_per_sm, &cand) != PKV_OK) continue;
-            cand.predicted_us = predict_us(&pol, &cand, lens);
+            choose_merge(&pol, &cand, lens);
             if (!have || cand.predicted_us < best.predicted_us) {
                 best = cand;
                 have = true;
@@ -232,7 +259,7 @@ extern "C" int pkv_plan_launches(const pkv_plan_t* plan) {
     switch (plan->variant) {
         case PKV_VARIANT_SINGLE: return 1;
         case PKV_VARIANT_SPLIT: return 1 + merge;
-        case PKV_VARIANT_WORKQUEUE: return 2 + merge;
+        case PKV_VARIANT_WORKQUEUE: return (plan->list_in_decode ? 1 : 2) + merge;
         default: return 0;
     }
 }

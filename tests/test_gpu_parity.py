@@ -297,12 +297,15 @@ def test_fused_and_separate_merge_match_oracle(name, seed, t):
     outs = []
     for variant, chunk in ((SPLIT, 1), (SPLIT, max(1, -(-pmax // 19))), (WQ, 2), (WQ, 16), (WQ, 64)):
         for fused in (1, 0):
-            plan = _with_merge(step.plan(variant, chunk), fused)
-            assert pkv.pkv_plan_launches(plan) == (1 if variant == SPLIT else 2) + (1 - fused)
-            out, _, status = step.run(plan)
-            assert status == 0, status
-            assert_close(out, ref, f"{name} seed {seed} step {t} variant {variant} c={chunk} fused={fused}")
-            outs.append(out.float())
+            for in_decode in ((1, 0) if variant == WQ else (0,)):
+                plan = _with_merge(step.plan(variant, chunk), fused)
+                plan.list_in_decode = in_decode
+                assert pkv.pkv_plan_launches(plan) == 1 + (1 - fused) + (variant == WQ and not in_decode)
+                out, _, status = step.run(plan)
+                assert status == 0, status
+                assert_close(out, ref, f"{name} seed {seed} step {t} variant {variant} c={chunk} fused={fused} "
+                                       f"list_in_decode={in_decode}")
+                outs.append(out.float())
     for o in outs[1:]:
         assert (o - outs[0]).abs().max().item() < 2e-3
 
@@ -313,6 +316,8 @@ def test_workqueue_decode_runs_twice_on_one_build():
     step = Step(make_trace("b8_bimodal", 5, steps=1), 0)
     ref = step.reference()
     plan = step.plan(WQ, 8)
+    plan.list_in_decode = 0  # run the builder's list
+    plan.fuse_merge = 1      # pkv_decode writes out itself
     ws = pkv.alloc_workspace(plan.ws_bytes)
     pkv.pkv_build_worklist(plan, step.problem, step.lens, ws)
     for call in range(3):
@@ -352,3 +357,27 @@ def test_all_rows_empty_write_zero_outputs():
             plan = _with_merge(step.plan(variant, 2), fused if variant != SINGLE else 0)
             out, _, status = step.run(plan)
             assert status == 0 and not out.isnan().any() and not out.any(), (variant, fused)
+
+
+@pytest.mark.parametrize("name,seed,chunk", [("b8_zipf", 5, 3), ("b8_uniform", 6, 16), ("stress", 5, 64),
+                                             ("tiny", 0, 1)])
+def test_list_derived_in_decode_matches_the_builder(name, seed, chunk):
+    """With list_in_decode the decode kernel publishes the same row offsets, split counts and task count as the
+    worklist builder (bit-exact), and both runs of the list give the oracle's output."""
+    tr = make_trace(name, seed, steps=1)
+    step = Step(tr, 0, poison=False)
+    plan = step.plan(WQ, chunk)
+    if tr.batch > pkv.PKV_MAX_ROWS_IN_DECODE:
+        pytest.skip("B above the in-decode row limit")
+    assert plan.list_in_decode == 1
+    _, ws, status = step.run(plan)
+    assert status == 0
+    B = tr.batch
+    got_off = ws[plan.off_row_off:plan.off_row_off + 4 * B].view(torch.int32).cpu().numpy()
+    got_spl = ws[plan.off_row_splits:plan.off_row_splits + 4 * B].view(torch.int32).cpu().numpy()
+    count = int(ws[:8].view(torch.int32).cpu().numpy()[1])
+    built = pkv.alloc_workspace(plan.ws_bytes)
+    pkv.pkv_build_worklist(plan, step.problem, step.lens, built)
+    _, off, spl, _ = read_worklist(plan, built)
+    assert np.array_equal(got_off, off) and np.array_equal(got_spl, spl)
+    assert count == len(oracle.worklist(step.lens_host, 16, tr.hkv, chunk))
