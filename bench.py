@@ -14,7 +14,9 @@ spin of --spin-us keeps the GPU busy while the host enqueues the step, so the CU
 around the decode kernel inside it) measure device time only, never a wait for the host. `value` = tokens / sum of
 step times. `e2e` repeats the same steps through the public API from pinned host buffers, timed on the host wall
 clock with a synchronize on both sides: per step one host->device copy of q, the block table, the lengths and the
-new token's K/V, the append of that K/V into its page slot, the step, and the device->host copy of out.
+new token's K/V, the step with that K/V appended into its page slot inside the decode, and the device->host copy
+of out. `traces.multilayer_...` runs the decode loop of an 8-layer model's attention on the B8 bimodal trace (one
+pkv_decode_step_append per layer per step, each layer with its own pools, no L2 flush: the layers' K/V exceed L2).
 `cpu_baseline` times the fp64 oracle on the host on a bounded sample of the same steps.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config b1_bucketed] ...
@@ -232,7 +234,7 @@ class Marshalled:
                        vp(s["bt"].data_ptr()), vp(s["lens"].data_ptr()), ctypes.c_float(scale), vp(ws.data_ptr()),
                        ws.numel(), vp(out.data_ptr()), st)
         self.merge = (pl, pr, vp(ws.data_ptr()), ws.numel(), vp(out.data_ptr()), st)
-        self.wq = plan.variant == pkv.PKV_VARIANT_WORKQUEUE
+        self.wq = plan.variant == pkv.PKV_VARIANT_WORKQUEUE and not plan.list_in_decode  # a builder launch
         self.separate_merge = plan.variant != pkv.PKV_VARIANT_SINGLE and not plan.fuse_merge
 
 
@@ -410,8 +412,8 @@ def run_reference(args):
 # ------------------------------------------------------------------------------------------------ our arm
 def run_e2e(pkv, torch, wl, idx, args, sms, flush, stream, dev):
     """The same steps through the public API from pinned host buffers, host wall clock with a synchronize on both
-    sides: one H2D copy of (q, block table, lengths, new K, new V), the append of the new token's K/V into its page
-    slot, pkv_plan + pkv_decode_step, one D2H copy of out."""
+    sides: one H2D copy of (q, block table, lengths, new K, new V), pkv_plan + pkv_decode_step_append (the new
+    token's K/V written into its page slot inside the decode), one D2H copy of out."""
     B, Hq, Hkv, d, ps = wl.B, wl.Hq, wl.Hkv, wl.d, wl.ps
     scale = 1.0 / math.sqrt(d)
     recs = []
@@ -424,9 +426,8 @@ def run_e2e(pkv, torch, wl, idx, args, sms, flush, stream, dev):
         used_index = {int(p): i for i, p in enumerate(tr.used_pages)}
         k_new = np.stack([tr.k_pages[used_index[int(new_phys[b])], int(new_slot[b])] for b in range(B)])
         v_new = np.stack([tr.v_pages[used_index[int(new_phys[b])], int(new_slot[b])] for b in range(B)])
-        rows = (new_phys.astype(np.int64) * ps + new_slot).astype(np.int64)
         parts = [s["q_host"].view(np.uint8).ravel(), k_new.view(np.uint8).ravel(), v_new.view(np.uint8).ravel(),
-                 s["bt_host"].view(np.uint8).ravel(), lens.view(np.uint8).ravel(), rows.view(np.uint8).ravel()]
+                 s["bt_host"].view(np.uint8).ravel(), lens.view(np.uint8).ravel()]
         # one pinned buffer, every part starting on a 256-byte boundary (the library wants 16-byte aligned q)
         sizes = [-(-p.size // 256) * 256 for p in parts]
         buf = np.zeros(sum(sizes), dtype=np.uint8)
@@ -453,17 +454,14 @@ def run_e2e(pkv, torch, wl, idx, args, sms, flush, stream, dev):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         dbuf[:packed.numel()].copy_(packed, non_blocking=True)
-        part = [dbuf[o[i]:o[i] + sizes[i]] for i in range(6)]
+        part = [dbuf[o[i]:o[i] + sizes[i]] for i in range(5)]
         q = part[0].view(torch.float16).view(B, Hq, d)
-        k_new = part[1].view(torch.float16).view(B, Hkv * d)
-        v_new = part[2].view(torch.float16).view(B, Hkv * d)
+        k_new = part[1].view(torch.float16).view(B, Hkv, d)
+        v_new = part[2].view(torch.float16).view(B, Hkv, d)
         bt = part[3].view(torch.int32).view(B, tr.max_pages)
         lens = part[4].view(torch.int32)
-        rows = part[5].view(torch.int64)
-        kpool.view(-1, Hkv * d).index_copy_(0, rows, k_new)
-        vpool.view(-1, Hkv * d).index_copy_(0, rows, v_new)
         plan = make_plan(pkv, problem, s["lens_host"], sms, args)
-        pkv.pkv_decode_step(plan, problem, q, kpool, vpool, bt, lens, scale, ws, out_d, stream)
+        pkv.pkv_decode_step_append(plan, problem, q, k_new, v_new, kpool, vpool, bt, lens, scale, ws, out_d, stream)
         out_h.copy_(out_d, non_blocking=True)
         torch.cuda.current_stream(dev).synchronize()
         times.append(time.perf_counter() - t0)
@@ -472,6 +470,80 @@ def run_e2e(pkv, torch, wl, idx, args, sms, flush, stream, dev):
     return {"value": B * len(times) / float(np.sum(times)), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": len(times), "us_per_step": 1e6 * float(np.mean(times)),
             "timing": "host wall clock per step, synchronize on both sides; includes pkv_plan"}
+
+
+def run_multilayer(pkv, torch, args, sms, dev, stream, peak, name="b8_bimodal", seed=5, layers=8):
+    """Decode loop of an 8-layer model's attention: per step and layer, the new token's K/V appended into that layer's
+    pools and the layer's attention, all inside pkv_decode_step_append. The layers share the trace's block table and
+    lengths; each has its own pools (sized to the trace, pages drawn by the trace's permutation) and the same
+    contents, so every layer reads its own K/V from HBM (the layers' K/V together exceed the L2)."""
+    import math as _m
+
+    from workloads import make_trace
+
+    tr = make_trace(name, seed)
+    B, Hq, Hkv, d, ps = tr.batch, tr.hq, tr.hkv, tr.d, tr.ps
+    idx = torch.from_numpy(tr.used_pages).to(dev)
+    kh, vh = torch.from_numpy(tr.k_pages).to(dev), torch.from_numpy(tr.v_pages).to(dev)
+    pools = []
+    for _ in range(layers):
+        k = torch.empty((tr.num_pages, ps, Hkv, d), dtype=torch.float16, device=dev)
+        v = torch.empty_like(k)
+        k.index_copy_(0, idx, kh)
+        v.index_copy_(0, idx, vh)
+        pools.append((k, v))
+    del kh, vh
+    problem = pkv.make_problem(B, Hq, Hkv, d, ps, tr.num_pages, tr.max_pages)
+    scale = 1.0 / _m.sqrt(d)
+    K = min(args.steps, tr.steps)
+    ts = strided(tr.steps, K)
+    used_index = {int(p): i for i, p in enumerate(tr.used_pages)}
+    steps = []
+    for t in ts:
+        lens = tr.seq_lens(t)
+        bt = tr.block_table(t)
+        phys = bt[np.arange(B), (lens - 1) // ps]
+        slot = (lens - 1) % ps
+        k_new = np.stack([tr.k_pages[used_index[int(phys[b])], int(slot[b])] for b in range(B)])
+        v_new = np.stack([tr.v_pages[used_index[int(phys[b])], int(slot[b])] for b in range(B)])
+        plan = pkv.pkv_plan(problem, lens, sms)
+        steps.append((plan, torch.from_numpy(tr.q(t)).to(dev), torch.from_numpy(k_new).to(dev),
+                      torch.from_numpy(v_new).to(dev), torch.from_numpy(bt).to(dev), torch.from_numpy(lens).to(dev),
+                      float(plan.kv_bytes)))
+    ws = pkv.alloc_workspace(max(st[0].ws_bytes for st in steps), dev)
+    out = torch.empty((B, Hq, d), dtype=torch.float16, device=dev)
+    lib = pkv.load()
+    vp = ctypes.c_void_p
+    calls = []
+    for plan, q, kn, vn, bt, ln, _ in steps:
+        calls.append([(ctypes.byref(plan), ctypes.byref(problem), vp(q.data_ptr()), vp(kn.data_ptr()),
+                       vp(vn.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()), vp(bt.data_ptr()), vp(ln.data_ptr()),
+                       ctypes.c_float(scale), vp(ws.data_ptr()), ws.numel(), vp(out.data_ptr()),
+                       vp(stream.cuda_stream)) for k, v in pools])
+    for layer_calls in calls[:2]:
+        for a in layer_calls:
+            _call(lib.pkv_decode_step_append, a, "pkv_decode_step_append")
+    torch.cuda.synchronize()
+    ev = []
+    spin = int(args.spin_us * 4 * 1e-6 * 2.0e9)
+    for layer_calls in calls:
+        torch.cuda._sleep(spin)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for a in layer_calls:
+            _call(lib.pkv_decode_step_append, a, "pkv_decode_step_append")
+        e1.record(stream)
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    status = pkv.pkv_read_status(ws)
+    step_us = np.array([a.elapsed_time(b) * 1e3 for a, b in ev])
+    kv = np.array([st[6] for st in steps]) * layers
+    return {"layers": layers, "trace": name, "seed": seed, "steps": K, "tokens_per_s": B * K / (step_us.sum() * 1e-6),
+            "step_us_mean": float(step_us.mean()), "layer_us_mean": float(step_us.mean()) / layers,
+            "step_frac": float(kv.sum() / (step_us.sum() * 1e-6)) / 1e9 / peak,
+            "launches_per_step": layers * pkv.pkv_plan_launches(steps[0][0]),
+            "variants_used": sorted({pkv.VARIANT_NAMES[st[0].variant] for st in steps}),
+            "l2": "not flushed: each step reads every layer's own pools", "device_status": int(status)}
 
 
 def run_ours(args):
@@ -586,6 +658,9 @@ def run_ours(args):
         r = time_workload(pkv, torch, wl, K, W, args, sms, dev, flush, stream)
         subs[name] = summarize(pkv, wl, r, peak)
         del wl, r
+    if names:
+        torch.cuda.empty_cache()
+        subs["multilayer_b8_bimodal_8layers"] = run_multilayer(pkv, torch, args, sms, dev, stream, peak)
     line["traces"] = subs
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -245,6 +245,20 @@ int pkv_decode_step(const pkv_plan_t* plan, const pkv_problem* problem, const vo
                     const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev, float scale,
                     void* ws, size_t ws_bytes, void* out, void* stream);
 
+/*
+ * One decode step of a model layer with the new token's K/V append fused into it (the step before attention in a
+ * decode loop; multi-layer decode calls it once per layer with that layer's pools). seq_lens_dev already counts the
+ * new token: row b's token L_b - 1 lives in slot (L_b - 1) % page_size of page block_table[b][(L_b - 1) / page_size],
+ * which the caller has allocated. k_new, v_new: [B][Hkv][d] fp16, 16-byte aligned, the token's K and V. The kernel
+ * that reads that page writes k_new / v_new into the pools' slot and uses them for this step's scores; rows with
+ * L_b = 0 append nothing. Otherwise as pkv_decode_step (plan, workspace, merge, errors). k_pool and v_pool are
+ * written (one 256-byte row per (row, KV head)).
+ */
+int pkv_decode_step_append(const pkv_plan_t* plan, const pkv_problem* problem, const void* q, const void* k_new,
+                           const void* v_new, void* k_pool, void* v_pool, const int32_t* block_table,
+                           const int32_t* seq_lens_dev, float scale, void* ws, size_t ws_bytes, void* out,
+                           void* stream);
+
 /* Synchronises `stream`, copies the workspace status word to *status and clears it on the device. */
 int pkv_read_status(void* ws, size_t ws_bytes, void* stream, uint32_t* status);
 

@@ -37,7 +37,7 @@ VARIANT_NAMES = {PKV_VARIANT_SINGLE: "single", PKV_VARIANT_SPLIT: "split", PKV_V
 EXPORTS = (
     "pkv_version", "pkv_strerror", "pkv_check_problem", "pkv_policy_default", "pkv_plan", "pkv_plan_fixed",
     "pkv_workspace_init", "pkv_build_worklist", "pkv_decode", "pkv_merge", "pkv_decode_step", "pkv_read_status",
-    "pkv_plan_launches", "pkv_decode_step_static",
+    "pkv_plan_launches", "pkv_decode_step_static", "pkv_decode_step_append",
 )
 
 PKV_STATIC_SCRATCH_BYTES = 16 << 20
@@ -123,6 +123,9 @@ def load(path: str | None = None):
         lib.pkv_read_status.argtypes = [_vp, ctypes.c_size_t, _vp, _P(ctypes.c_uint32)]
         lib.pkv_plan_launches.restype = ctypes.c_int
         lib.pkv_plan_launches.argtypes = [_P(Plan)]
+        lib.pkv_decode_step_append.restype = ctypes.c_int
+        lib.pkv_decode_step_append.argtypes = [_P(Plan), _P(Problem), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                               ctypes.c_float, _vp, ctypes.c_size_t, _vp, _vp]
         lib.pkv_decode_step_static.restype = ctypes.c_int
         lib.pkv_decode_step_static.argtypes = [_P(Plan), _P(Problem), _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp,
                                                _vp, _vp]

@@ -18,7 +18,8 @@ from ._lib import (PKV_VARIANT_SINGLE, PKV_VARIANT_SPLIT, PKV_VARIANT_WORKQUEUE,
 __all__ = [
     "Problem", "Plan", "Policy", "pkv_version", "pkv_strerror", "pkv_check_problem", "pkv_policy_default",
     "pkv_plan", "pkv_plan_fixed", "pkv_workspace_init", "pkv_build_worklist", "pkv_decode", "pkv_merge",
-    "pkv_decode_step", "pkv_read_status", "pkv_plan_launches", "pkv_decode_step_static", "make_problem",
+    "pkv_decode_step", "pkv_read_status", "pkv_plan_launches", "pkv_decode_step_static", "pkv_decode_step_append",
+    "make_problem",
     "alloc_workspace", "decode",
     "PKV_VARIANT_SINGLE", "PKV_VARIANT_SPLIT", "PKV_VARIANT_WORKQUEUE",
 ]
@@ -132,6 +133,17 @@ def pkv_merge(plan: Plan, problem: Problem, ws: torch.Tensor, out: torch.Tensor,
 def pkv_decode_step(plan, problem, q, k_pool, v_pool, block_table, seq_lens, scale, ws, out, stream=None) -> None:
     check(load().pkv_decode_step(*_decode_args(plan, problem, q, k_pool, v_pool, block_table, seq_lens, scale, ws,
                                                out, stream)), "pkv_decode_step")
+
+
+def pkv_decode_step_append(plan, problem, q, k_new, v_new, k_pool, v_pool, block_table, seq_lens, scale, ws, out,
+                           stream=None) -> None:
+    """pkv_decode_step with the new token's K/V ([B, Hkv, d] fp16) appended into the pools inside the decode."""
+    check(load().pkv_decode_step_append(
+        ctypes.byref(plan), ctypes.byref(problem), _ptr(q, torch.float16, "q"), _ptr(k_new, torch.float16, "k_new"),
+        _ptr(v_new, torch.float16, "v_new"), _ptr(k_pool, torch.float16, "k_pool"),
+        _ptr(v_pool, torch.float16, "v_pool"), _ptr(block_table, torch.int32, "block_table"),
+        _ptr(seq_lens, torch.int32, "seq_lens"), ctypes.c_float(scale), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+        _ptr(out, torch.float16, "out"), _stream(stream)), "pkv_decode_step_append")
 
 
 def pkv_decode_step_static(plan, problem, q, k_pool, v_pool, block_table, seq_lens, scale, out, status=None,

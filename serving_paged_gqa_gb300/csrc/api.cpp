@@ -163,11 +163,13 @@ int check_decode_args(const pkv_plan_t* plan, const pkv_problem* pr, const void*
     return PKV_OK;
 }
 
-int decode_step(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_pool,
-                const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev, float scale, void* ws,
-                size_t ws_bytes, void* out, void* stream, bool clear_counters) {
+int decode_step(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_new, const void* v_new,
+                const void* k_pool, const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev,
+                float scale, void* ws, size_t ws_bytes, void* out, void* stream, bool clear_counters) {
     int rc = check_decode_args(plan, pr, q, k_pool, v_pool, block_table, seq_lens_dev, scale, ws, ws_bytes, out);
     if (rc != PKV_OK) return rc;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_E_NULLPTR;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return PKV_E_ALIGN;
     if (clear_counters) {
         const size_t n = 4 * (size_t)pr->batch * pr->num_kv_heads;
         if (n > 0 && cudaMemsetAsync(at<char>(ws, plan->off_counters), 0, n, static_cast<cudaStream_t>(stream)) !=
@@ -178,7 +180,8 @@ int decode_step(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, co
         rc = pkv_build_worklist(plan, pr, seq_lens_dev, ws, ws_bytes, stream);
         if (rc != PKV_OK) return rc;
     }
-    rc = pkv_decode(plan, pr, q, k_pool, v_pool, block_table, seq_lens_dev, scale, ws, ws_bytes, out, stream);
+    rc = decode_launch(plan, pr, q, k_new, v_new, k_pool, v_pool, block_table, seq_lens_dev, scale, ws, ws_bytes, out,
+                       stream);
     if (rc != PKV_OK) return rc;
     return pkv_merge(plan, pr, ws, ws_bytes, out, stream);
 }
@@ -188,8 +191,17 @@ int decode_step(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, co
 extern "C" int pkv_decode(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_pool,
                           const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev, float scale,
                           void* ws, size_t ws_bytes, void* out, void* stream) {
+    return decode_launch(plan, pr, q, nullptr, nullptr, k_pool, v_pool, block_table, seq_lens_dev, scale, ws, ws_bytes,
+                         out, stream);
+}
+
+int pkv::decode_launch(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_new,
+                       const void* v_new, const void* k_pool, const void* v_pool, const int32_t* block_table,
+                       const int32_t* seq_lens_dev, float scale, void* ws, size_t ws_bytes, void* out, void* stream) {
     int rc = check_decode_args(plan, pr, q, k_pool, v_pool, block_table, seq_lens_dev, scale, ws, ws_bytes, out);
     if (rc != PKV_OK) return rc;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_E_NULLPTR;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return PKV_E_ALIGN;
     // A workqueue plan may hold no task while its rows still need an output (every row empty); other plans have
     // tasks whenever B > 0.
     if (pr->batch == 0) return PKV_OK;
@@ -202,6 +214,8 @@ extern "C" int pkv_decode(const pkv_plan_t* plan, const pkv_problem* pr, const v
     p.q = q;
     p.k_pool = k_pool;
     p.v_pool = v_pool;
+    p.k_new = k_new;
+    p.v_new = v_new;
     p.block_table = block_table;
     p.seq_lens = seq_lens_dev;
     p.out = out;
@@ -257,8 +271,17 @@ extern "C" int pkv_merge(const pkv_plan_t* plan, const pkv_problem* pr, void* ws
 extern "C" int pkv_decode_step(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_pool,
                                const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev,
                                float scale, void* ws, size_t ws_bytes, void* out, void* stream) {
-    return decode_step(plan, pr, q, k_pool, v_pool, block_table, seq_lens_dev, scale, ws, ws_bytes, out, stream,
-                       false);
+    return decode_step(plan, pr, q, nullptr, nullptr, k_pool, v_pool, block_table, seq_lens_dev, scale, ws, ws_bytes,
+                       out, stream, false);
+}
+
+extern "C" int pkv_decode_step_append(const pkv_plan_t* plan, const pkv_problem* pr, const void* q,
+                                      const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                                      const int32_t* block_table, const int32_t* seq_lens_dev, float scale, void* ws,
+                                      size_t ws_bytes, void* out, void* stream) {
+    if (pr && pr->batch > 0 && (!k_new || !v_new)) return PKV_E_NULLPTR;
+    return decode_step(plan, pr, q, k_new, v_new, k_pool, v_pool, block_table, seq_lens_dev, scale, ws, ws_bytes, out,
+                       stream, false);
 }
 
 extern "C" int pkv_read_status(void* ws, size_t ws_bytes, void* stream, uint32_t* status) {

@@ -130,6 +130,11 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// Physical page of logical page `lp` of row b (the appended token's page; read once per (row, KV head)).
+__device__ __forceinline__ int32_t logical_page_phys(const DecodeParams& p, int b, int lp) {
+    return __ldg(p.block_table + (size_t)b * p.max_pages + lp);
+}
+
 __device__ __forceinline__ void store_half4(__half* dst, float4 v, float scale) {
     uint2 pk;
     pk.x = pack_half2(v.x * scale, v.y * scale);
@@ -669,6 +674,26 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
                     }
                     __syncwarp();
                 }
+                const bool append = p.k_new != nullptr && (spb + i) * kPageSize + nvalid == slen;
+                if (append) {
+                    // The page holds the row's newest token (slot nvalid - 1), appended in this step: its K and V
+                    // rows of KV head sh come from k_new / v_new. Lane l moves 16 bytes: pool l / 16 (K, V), box
+                    // (l / 8) % 2 (columns 0-63, 64-127), chunk l % 8. Into the staged page (swizzled) for this
+                    // step's scores, and into the pool slot for later steps; no other task reads these bytes.
+                    const int r = nvalid - 1, pool = lane >> 4, half = (lane >> 3) & 1, chunk = lane & 7;
+                    const size_t src = ((size_t)sb * Hkv + sh) * kHeadDim + half * 64 + chunk * 8;
+                    const int4 val = *reinterpret_cast<const int4*>(
+                        static_cast<const __half*>(pool ? p.v_new : p.k_new) + src);
+                    uint8_t* stage = smem + L::off_stage + st * kStageBytes + (2 * pool + half) * kBoxBytes;
+                    *reinterpret_cast<int4*>(stage + r * 128 + ((chunk ^ (r & 7)) << 4)) = val;
+                    const int32_t phys = logical_page_phys(p, sb, spb + i);
+                    if (phys >= 0 && phys < p.num_pages) {
+                        __half* dst = const_cast<__half*>(static_cast<const __half*>(pool ? p.v_pool : p.k_pool)) +
+                                      (((size_t)phys * kPageSize + r) * Hkv + sh) * kHeadDim + half * 64 + chunk * 8;
+                        *reinterpret_cast<int4*>(dst) = val;
+                    }
+                    __syncwarp();
+                }
                 // S^T = K Q^T: rows = the 16 tokens, columns = 8 heads per tile, k = head_dim in 8 steps of 16
                 float sc[kNT][4];
 #pragma unroll
@@ -728,7 +753,7 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
 #pragma unroll
                     for (int nt = 0; nt < kNT; ++nt) mma_16816(o[nt][d], a0, a1, a2, a3, pb0[nt], pb1[nt]);
                 }
-                if (nvalid < kPageSize) fence_proxy_async_smem();  // zero stores before the next TMA write
+                if (nvalid < kPageSize || append) fence_proxy_async_smem();  // our stores before the next TMA write
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[st]);
             }

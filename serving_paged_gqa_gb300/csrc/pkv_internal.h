@@ -26,6 +26,8 @@ struct DecodeParams {
     const void* q;
     const void* k_pool;
     const void* v_pool;
+    const void* k_new;     // [B][Hkv][d] fp16: the token appended this step (NULL: nothing to append)
+    const void* v_new;
     const int32_t* block_table;
     const int32_t* seq_lens;
     void* out;             // fp16 [B][Hq][d] (single-pass only)
@@ -74,10 +76,15 @@ int check_decode_args(const pkv_plan_t* plan, const pkv_problem* pr, const void*
                       void* ws, size_t ws_bytes, void* out);
 
 // build (workqueue) + decode + merge on one stream after validating every argument up front; with clear_counters
-// the workspace's arrival counters are zeroed first.
-int decode_step(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_pool, const void* v_pool,
-                const int32_t* block_table, const int32_t* seq_lens_dev, float scale, void* ws, size_t ws_bytes,
-                void* out, void* stream, bool clear_counters);
+// the workspace's arrival counters are zeroed first; k_new / v_new (both or neither) are appended inside the decode.
+int decode_step(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_new, const void* v_new,
+                const void* k_pool, const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev,
+                float scale, void* ws, size_t ws_bytes, void* out, void* stream, bool clear_counters);
+
+// pkv_decode with the appended token (k_new / v_new may be NULL).
+int decode_launch(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_new, const void* v_new,
+                  const void* k_pool, const void* v_pool, const int32_t* block_table, const int32_t* seq_lens_dev,
+                  float scale, void* ws, size_t ws_bytes, void* out, void* stream);
 
 // Dynamic shared memory of the decode kernel for a group size (0 if unsupported).
 int decode_smem_bytes(int group);

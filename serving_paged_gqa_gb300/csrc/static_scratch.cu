@@ -62,8 +62,8 @@ extern "C" int pkv_decode_step_static(const pkv_plan_t* plan, const pkv_problem*
     // The fused merge's arrival counters must start at zero: a completed step leaves them at zero, but a step
     // that gave up (a timeout, a truncated task list) may not, and no caller can re-initialise this array, so
     // every call clears them first.
-    rc = decode_step(plan, problem, q, k_pool, v_pool, block_table, seq_lens_dev, scale, ws, PKV_STATIC_SCRATCH_BYTES,
-                     out, stream, true);
+    rc = decode_step(plan, problem, q, nullptr, nullptr, k_pool, v_pool, block_table, seq_lens_dev, scale, ws,
+                     PKV_STATIC_SCRATCH_BYTES, out, stream, true);
     if (rc != PKV_OK) return rc;
     // The status word is the only other part of the array a step reads before writing it: hand it over, then
     // clear it so the next call starts from zero.

@@ -381,3 +381,40 @@ def test_list_derived_in_decode_matches_the_builder(name, seed, chunk):
     _, off, spl, _ = read_worklist(plan, built)
     assert np.array_equal(got_off, off) and np.array_equal(got_spl, spl)
     assert count == len(oracle.worklist(step.lens_host, 16, tr.hkv, chunk))
+
+
+# ------------------------------------------------------------------------------------------- fused KV append
+@pytest.mark.parametrize("name,seed,t", [("tiny", 0, 0), ("b8_bimodal", 5, 7), ("b1_bucketed", 9, 20),
+                                         ("b8_zipf", 6, 3), ("b4_bimodal", 8, 16)])
+def test_fused_kv_append_matches_oracle_and_fills_the_slot(name, seed, t):
+    """pkv_decode_step_append with the new token's K/V only in k_new / v_new (its pool slots hold NaN): the output
+    matches the oracle on the full pools and the slots end up holding the token bit for bit, for every schedule and
+    both merges (t = 16 on B4 / t = 0 on tiny put the new token in a full page, others in a partial one)."""
+    tr = make_trace(name, seed, steps=t + 1)
+    step = Step(tr, t, poison=False)
+    ref = step.reference()
+    B = tr.batch
+    rows = torch.arange(B)
+    L = torch.from_numpy(step.lens_host.astype(np.int64))
+    phys = step.bt.cpu()[rows, (L - 1) // 16].cuda().long()
+    slot = ((L - 1) % 16).cuda()
+    k_new = step.k[phys, slot].clone()
+    v_new = step.v[phys, slot].clone()
+    pmax = int(tr.pages(t).max())
+    plans = [(SINGLE, 1, 0), (SPLIT, max(1, -(-pmax // 8)), 0), (SPLIT, max(1, -(-pmax // 8)), 1), (WQ, 4, 0),
+             (WQ, 16, 1)]
+    for variant, chunk, fused in plans:
+        step.k[phys, slot] = float("nan")
+        step.v[phys, slot] = float("nan")
+        plan = step.plan(variant, chunk)
+        if variant != SINGLE:
+            plan.fuse_merge = fused
+        ws = pkv.alloc_workspace(plan.ws_bytes)
+        out = torch.full_like(step.q, float("nan"))
+        pkv.pkv_decode_step_append(plan, step.problem, step.q, k_new, v_new, step.k, step.v, step.bt, step.lens,
+                                   step.scale, ws, out)
+        torch.cuda.synchronize()
+        assert pkv.pkv_read_status(ws) == 0
+        assert_close(out, ref, f"{name} append variant {variant} c={chunk} fused={fused}")
+        assert torch.equal(step.k[phys, slot].view(torch.int16), k_new.view(torch.int16))
+        assert torch.equal(step.v[phys, slot].view(torch.int16), v_new.view(torch.int16))
