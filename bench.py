@@ -546,6 +546,69 @@ def run_multilayer(pkv, torch, args, sms, dev, stream, peak, name="b8_bimodal", 
             "l2": "not flushed: each step reads every layer's own pools", "device_status": int(status)}
 
 
+def run_schedules(pkv, torch, args, sms, dev, flush, stream, name="b8_bimodal"):
+    """The pages' comparison on held-out bimodal B8 steps: exact-length buckets (one split grid + merge per distinct
+    length, rows sorted by length), the padded split grid and the compact workqueue, each as the planner sizes it:
+    device time per step, launches per step and partial-state bytes per step."""
+    from serving_paged_gqa_gb300 import schedules
+
+    seeds = [int(x) for x in args.seeds.split(",")]
+    wl = Workload(torch, name, seeds, dev, args.pool_pages)
+    scale = 1.0 / math.sqrt(wl.d)
+    spin = int(2 * args.spin_us * 1e-6 * 2.0e9)
+    res = {k: {"us": [], "launches": [], "state_bytes": []} for k in ("exact_buckets", "padded_grid", "workqueue")}
+    same_c = []  # partial-state bytes of the padded grid cut like the workqueue (the pages' like-for-like counter)
+    for j in strided(len(wl.steps), args.steps):
+        s = wl.steps[j]
+        _, kpool, vpool = wl.traces[s["trace"]]
+        problem = wl.problem(pkv, s["trace"])
+        order = np.argsort(s["lens_host"], kind="stable")
+        oi = torch.from_numpy(order).to(dev)
+        q_s, bt_s, ln_s = s["q"][oi].contiguous(), s["bt"][oi].contiguous(), s["lens"][oi].contiguous()
+        buckets = schedules.ExactLengthBuckets(pkv, problem, s["lens_host"][order], sms)
+        padded = schedules.padded_grid_plan(pkv, problem, s["lens_host"], sms)
+        work = schedules.workqueue_plan(pkv, problem, s["lens_host"], sms)
+        same_c.append(schedules.state_bytes(pkv.pkv_plan_fixed(problem, s["lens_host"], sms, pkv.PKV_VARIANT_SPLIT,
+                                                               work.chunk_pages)))
+        ws = pkv.alloc_workspace(max(buckets.ws_bytes, padded.ws_bytes, work.ws_bytes), dev)
+        out = torch.empty_like(s["q"])
+        runs = {"exact_buckets": (lambda: buckets.run(q_s, kpool, vpool, bt_s, ln_s, scale, ws, out, stream),
+                                  buckets.launches(), buckets.state_bytes()),
+                "padded_grid": (lambda: pkv.pkv_decode_step(padded, problem, s["q"], kpool, vpool, s["bt"], s["lens"],
+                                                            scale, ws, out, stream),
+                                pkv.pkv_plan_launches(padded), schedules.state_bytes(padded)),
+                "workqueue": (lambda: pkv.pkv_decode_step(work, problem, s["q"], kpool, vpool, s["bt"], s["lens"],
+                                                          scale, ws, out, stream),
+                              pkv.pkv_plan_launches(work), schedules.state_bytes(work))}
+        for key, (fn, launches, sb) in runs.items():
+            fn()
+            ev = []
+            for _ in range(3):
+                flush()
+                torch.cuda._sleep(spin)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                ev.append((e0, e1))
+            torch.cuda.synchronize()
+            res[key]["us"].append(float(np.median([a.elapsed_time(b) * 1e3 for a, b in ev])))
+            res[key]["launches"].append(launches)
+            res[key]["state_bytes"].append(sb)
+        if pkv.pkv_read_status(ws) != 0:
+            raise SystemExit("device status set in the schedule comparison")
+    out = {k: {"us_per_step": float(np.mean(v["us"])), "launches_per_step": float(np.mean(v["launches"])),
+               "state_mb_per_step": float(np.mean(v["state_bytes"])) / 1e6} for k, v in res.items()}
+    out["workqueue_vs_exact_buckets_time"] = out["workqueue"]["us_per_step"] / out["exact_buckets"]["us_per_step"]
+    out["padded_grid_at_workqueue_split_size_state_mb_per_step"] = float(np.mean(same_c)) / 1e6
+    out["workqueue_vs_padded_state_traffic_same_split_size"] = (
+        out["workqueue"]["state_mb_per_step"] / out["padded_grid_at_workqueue_split_size_state_mb_per_step"] - 1.0)
+    out["pages"] = ("RTX 3060: 16.00 -> 2.00 launches per step (exact buckets -> workqueue), merge-state traffic "
+                    "about -37 %")
+    out["steps"] = args.steps
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -661,6 +724,8 @@ def run_ours(args):
     if names:
         torch.cuda.empty_cache()
         subs["multilayer_b8_bimodal_8layers"] = run_multilayer(pkv, torch, args, sms, dev, stream, peak)
+        torch.cuda.empty_cache()
+        subs["schedules_b8_bimodal"] = run_schedules(pkv, torch, args, sms, dev, flush, stream)
     line["traces"] = subs
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -64,3 +64,33 @@ def test_merge_state_bytes_hand_derived():
     # a page count that is not a multiple of c rounds up: L = [33] is 3 pages, c = 2 gives 2 splits
     mb = oracle.merge_state_bytes([33], 16, 4, 4, 2)
     assert mb == {"rect": 2 * (1 * 4 * 2) * 520, "workqueue": 2 * (4 * 2) * 520}
+
+
+def test_library_schedules_reproduce_the_launch_fanout_and_state_counters():
+    """The library's comparison schedules (serving_paged_gqa_gb300.schedules) count what the oracle counts: on the
+    held-out bimodal B8 traces, exact-length buckets launch a split kernel and a merge kernel per distinct length
+    (16.00 per step, the pages' value) and the workqueue with its separate merge 2.00; the partial-state bytes of the
+    padded grid and the workqueue at a common split size equal the oracle's merge_state_bytes."""
+    import serving_paged_gqa_gb300 as pkv
+    from serving_paged_gqa_gb300 import build, schedules
+
+    build.build()
+    g = _golden()
+    buckets, wq = [], []
+    for seed in range(5, 10):
+        tr = make_trace("b8_bimodal", seed)
+        problem = pkv.make_problem(tr.batch, tr.hq, tr.hkv, tr.d, tr.ps, tr.num_pages, tr.max_pages)
+        for t in range(0, tr.steps, 8):
+            lens = np.sort(tr.seq_lens(t))
+            buckets.append(schedules.ExactLengthBuckets(pkv, problem, lens, 152).launches())
+            plan = schedules.workqueue_plan(pkv, problem, lens, 152)
+            plan.fuse_merge = 0  # decode kernel + merge kernel (the list is derived inside the decode)
+            wq.append(pkv.pkv_plan_launches(plan))
+            for c in (8, 32):
+                rect = pkv.pkv_plan_fixed(problem, lens, 152, pkv.PKV_VARIANT_SPLIT, c)
+                work = pkv.pkv_plan_fixed(problem, lens, 152, pkv.PKV_VARIANT_WORKQUEUE, c)
+                ref = oracle.merge_state_bytes(lens, 16, tr.hq, tr.hkv, c)
+                assert schedules.state_bytes(rect) == ref["rect"]
+                assert schedules.state_bytes(work) == ref["workqueue"]
+    assert round(float(np.mean(buckets)), 2) == g["exact_buckets"]
+    assert round(float(np.mean(wq)), 2) == g["workqueue"]

@@ -418,3 +418,23 @@ def test_fused_kv_append_matches_oracle_and_fills_the_slot(name, seed, t):
         assert_close(out, ref, f"{name} append variant {variant} c={chunk} fused={fused}")
         assert torch.equal(step.k[phys, slot].view(torch.int16), k_new.view(torch.int16))
         assert torch.equal(step.v[phys, slot].view(torch.int16), v_new.view(torch.int16))
+
+
+def test_exact_length_bucket_schedule_matches_oracle():
+    """The exact-length-bucket comparison schedule (one split grid + merge per distinct length, rows sorted by
+    length) computes the same attention."""
+    from serving_paged_gqa_gb300 import schedules
+
+    step = Step(_Lens([40, 300, 40, 17, 300, 0, 1000, 17]).trace, 0)
+    ref = step.reference()
+    order = np.argsort(step.lens_host, kind="stable")
+    idx = torch.from_numpy(order).cuda()
+    sched = schedules.ExactLengthBuckets(pkv, step.problem, step.lens_host[order], step.sms)
+    assert sched.launches() == 2 * 4  # lengths 17, 40, 300, 1000
+    ws = pkv.alloc_workspace(sched.ws_bytes)
+    out = torch.full_like(step.q, float("nan"))
+    sched.run(step.q[idx].contiguous(), step.k, step.v, step.bt[idx].contiguous(), step.lens[idx].contiguous(),
+              step.scale, ws, out)
+    torch.cuda.synchronize()
+    assert pkv.pkv_read_status(ws) == 0
+    assert_close(out, ref[order], "exact-length buckets")
