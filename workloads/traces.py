@@ -4,8 +4,9 @@ Source: "PersistentKV: Page-Aware Decode Scheduling for Long-Context LLM Serving
 2606.26666). The abstract fixes the shapes (FP16, page size 16, Hq=32, Hkv=8, d=128) and names the trace families
 (B1 bucketed long context; B8 bimodal, uniform and Zipf-like; the B4 bimodal boundary case); the gist.science
 technical summary, "Evaluatieprotocol", says the traces are synthetic and built to isolate context length, active
-batch size and length raggedness. The pages give no distribution parameters; the ones below are the plain readings
-used throughout this repository (see the input recipe in the design notes).
+batch size and length raggedness. The pages give no distribution parameters; the ones below are plain readings:
+bimodal rows are half short (U[256, 1024]) then half long (U[16384, 32768]); Zipf-like lengths are 256 * k with k
+drawn from Zipf(1.1) truncated to 1..128; values are fp16 N(0, 1) through a 16-bit quantile table.
 
 Everything is seeded. Values are drawn with numpy's PCG64 through ``SeedSequence([seed, stream...])`` so the same
 seed gives the same trace on any machine. Nothing here computes attention.
