@@ -111,6 +111,23 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def max_over_ranks(x: float, dev) -> float:
+    """The largest x over the ranks of the default process group (x itself without one)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, slowest_ms: float) -> float:
+    """Units of all ranks (replicas, the same work each) over the slowest rank's timed milliseconds, per second."""
+    return units_per_rank * world / (slowest_ms * 1e-3)
+
+
 def strided(n: int, k: int) -> list[int]:
     """k step indices spread evenly over n steps."""
     return [(i * n) // k for i in range(k)]
@@ -648,11 +665,7 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.finish()
-    total_ms = float(r["step_ms"].sum())
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(r["step_ms"].sum()), dev)
     head = summarize(pkv, wl, r, peak)
 
     # ---- synchronized wall time per step (the pages' protocol): plan + launches + sync, flush outside
@@ -696,7 +709,7 @@ def run_ours(args):
               "variants_used": head["variants_used"], "chunk_pages_min_max": head["chunk_pages_min_max"],
               "splits_min_max": head["splits_min_max"], "parallelism": f"replicas x{world}"}
     line = {
-        "metric": METRIC, "value": K * B * world / (total_ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": whole_job_rate(K * B, world, total_ms), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic", "impl": "ours", "config": config,
         "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peak, "unit": "GB/s", "frac": dec_gbs / peak,
