@@ -11,24 +11,29 @@
 // CTA layout (persistent over tasks; grid = one wave of resident CTAs):
 //   warp NCW+2  scheduler: takes tasks (split / single: a static stride over the (b, h, s) task space; workqueue: an
 //               atomic queue head over the built list in the same order,
-//               after waiting for the builder grid), fetches the row length and the task's first 32 block-table
-//               entries together, publishes both in a shared-memory task slot, then bulk-copies the G query rows of
-//               the task into the slot (completion on a separate barrier, so the loader never waits for q);
+//               after waiting for the builder grid), bulk-copies the G query rows of the task into a shared-memory
+//               task slot (completion on their own barrier), fetches the row length and the task's first 32
+//               block-table entries together and publishes them in the slot. With the merge fused it also publishes
+//               merge tasks that the epilogue warp requests, and ends only after the epilogue has seen every task;
 //   warp NCW+1  loader: per page, one elected lane issues four 3-D TMA tensor copies (K and V of KV head h, each as
 //               two 64-column boxes of the page's 16 token rows, 128-byte swizzled) into a ring stage, counted in
-//               bytes on the stage's mbarrier; block-table entries past the slot's 32 are read one chunk ahead;
+//               bytes on the stage's mbarrier; block-table entries past the slot's 32 are read one chunk ahead. For a
+//               static plan it reads its first task's entries itself before the CTA barrier. A merge task's partial
+//               states go through the same ring, 16 states (8 KB of acc) per stage, by bulk copies;
 //   warps 0..NCW-1 consumers: page j of the CTA's page sequence (counted across tasks) lives in stage j % NS and
 //               goes to warp j % NCW (NS % NCW == 0, so a stage always has the same consumer). The products are
 //               taken transposed, so the 16 tokens (scores) and the head dimension (output) fill the 16-row side of
 //               mma.sync m16n8k16 and the G query heads the 8-column side: S^T = K Q^T (8 MMAs per page for G <= 8),
 //               masking of slots past the row length, online softmax in base 2 per head column, P^T rebuilt in the
 //               B-operand layout with four shuffles, O^T += V^T P^T (8 MMAs). At the end of a task each warp hands
-//               its (m, l, O) to the epilogue warp through a double-buffered shared-memory slot and moves on.
-//   warp NCW    epilogue: combines the NCW warps' partials of a task and writes the normalised output (single pass)
-//               or the partial state (m, l, acc) of each query head. With the merge fused it then counts the task
-//               in the (b, h) arrival counter; the last of the S_b tasks of (b, h) to arrive bulk-copies the S_b * G
-//               states of (b, h) from L2 through a two-buffer shared-memory chunk ring, merges them exactly and
-//               writes out, then re-arms the counter. Nobody waits for another CTA.
+//               its (m, l, O) to the epilogue warp through a double-buffered shared-memory slot and moves on. In a
+//               merge task a warp folds the states of its stages into a running (M, D, A) per query head instead.
+//   warp NCW    epilogue: combines the NCW warps' partials of a task and writes the normalised output (single pass,
+//               merge task) or the partial state (m, l, acc) of each query head. With the merge fused it then counts
+//               the task in the (b, h) arrival counter; the last of the S_b tasks of (b, h) to arrive re-arms the
+//               counter and asks the scheduler (a shared-memory mailbox) for a merge task of (b, h), which the
+//               loader, the consumers and this warp then run like any task: all of the pair's states are in flight
+//               at once through the ring. Nobody waits for another CTA.
 // Every wait is bounded (global timer); on timeout the kernel sets PKV_STATUS_TIMEOUT in the workspace, the other
 // warps see an abort flag, every warp that issued bulk copies waits (bounded) for them, and the CTA returns.
 #include <cuda_fp16.h>
@@ -43,20 +48,32 @@ constexpr int kBoxBytes = kPageSize * 128;   // one TMA box: 16 token rows x 64 
 constexpr int kStageBytes = 4 * kBoxBytes;   // K columns 0-63, K 64-127, V 0-63, V 64-127
 constexpr int kCombRow = kHeadDim + 4;       // floats per partial output row (132: rows land 4 banks apart)
 constexpr int kSlotEntries = 32;             // block-table entries the scheduler prefetches per task
-constexpr int kMergeChunk = 16;              // partial states per merge chunk (8 KB of acc)
+constexpr int kMergeStates = kStageBytes / (kHeadDim * 4);  // partial states per ring stage in a merge task (16)
+constexpr int kMailbox = 32;                 // merge requests the epilogue may post ahead of the scheduler
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Task kinds: the pages of a task, or the merge of the split states of one (row, KV head) pair.
+constexpr int kKindPages = 0;
+constexpr int kKindMerge = 1;
+
 struct TaskSlot {
     int32_t b, h, s, task;                  // task: canonical index; the task's states are task * G + g
     int32_t page_begin, npages, seq_len, nsplit;  // nsplit: tasks of (b, h) (arrivals of the fused merge; 0 = none)
+    int32_t kind, pad0, pad1, pad2;         // merge: task = the pair's first task, npages = state chunks
     int32_t ent[kSlotEntries];              // physical page of logical page page_begin + i (i < min(npages, 32))
 };
 
 // What the epilogue warp needs to know about a task (written by consumer warp 0; npages < 0 ends the CTA).
 struct EpiHeader {
-    int32_t b, h, s, task, nsplit, npages, pad0, pad1;
+    int32_t b, h, s, task, nsplit, npages, kind, pad;
+};
+
+// A merge the epilogue warp asks the scheduler for: the pair (b, h) whose nsplit tasks from `first` on have all
+// written their states.
+struct MergeReq {
+    int32_t b, h, first, nsplit;
 };
 
 template <int G, int NCW, int NS, int NTS>
@@ -64,18 +81,17 @@ struct Layout {
     static constexpr int kNT = (G + 7) / 8;  // 8-head column tiles of the MMAs
     static constexpr int kQRowsBytes = ((G * kRowBytes + 127) / 128) * 128;
     static constexpr int kCombFloats = NCW * G * kCombRow;  // one slot: every consumer warp's O rows
-    static constexpr int kMergeBufs = 2;                    // merge chunks in flight
     static constexpr int off_stage = 0;  // 1024-byte aligned (128-byte swizzle atom)
     static constexpr int off_q = off_stage + NS * kStageBytes;
-    static constexpr int off_mbuf = off_q + NTS * kQRowsBytes;             // 2 merge chunks (bulk copy targets)
-    static constexpr int off_comb = off_mbuf + kMergeBufs * kMergeChunk * kHeadDim * 4;
+    static constexpr int off_comb = off_q + NTS * kQRowsBytes;
     static constexpr int off_comb_ml = off_comb + 2 * kCombFloats * 4;    // float2 (m, l) per slot/warp/head
     static constexpr int off_ehdr = off_comb_ml + 2 * NCW * G * 8;
     static constexpr int off_rows = off_ehdr + 2 * (int)sizeof(EpiHeader);  // in-decode list: off, S_b, L_b per row
-    static constexpr int off_slots = off_rows + 3 * PKV_MAX_ROWS_IN_DECODE * 4;
+    static constexpr int off_mreq = off_rows + 3 * PKV_MAX_ROWS_IN_DECODE * 4;  // merge-request mailbox
+    static constexpr int off_slots = off_mreq + kMailbox * (int)sizeof(MergeReq);
     static constexpr int off_bars = ((off_slots + NTS * (int)sizeof(TaskSlot) + 15) / 16) * 16;
-    static constexpr int nbars = 2 * NS + 3 * NTS + 4 + kMergeBufs;
-    static constexpr int off_flag = off_bars + nbars * 8;
+    static constexpr int nbars = 2 * NS + 3 * NTS + 4;
+    static constexpr int off_flag = off_bars + nbars * 8;  // abort flag, requests posted, requests taken, verdicts
     static constexpr int used = off_flag + 16;
     static constexpr int total = used + 1024;  // slack to align the base to 1024 bytes
 };
@@ -142,80 +158,138 @@ __device__ __forceinline__ void store_half4(__half* dst, float4 v, float scale) 
     *reinterpret_cast<uint2*>(dst) = pk;
 }
 
-// ---------------------------------------------------------------------------------------------- epilogue warp
-// Exact log-sum-exp merge of the nsplit partial states of every query head of the task group starting at task
-// `first`: out_g = sum_s e^(m_s - M) acc_s / sum_s e^(m_s - M) l_s over states with l_s > 0, with a running maximum
-// so the states are read once. The states of (b, h) are contiguous ((s, g) order, g fastest); they were written by
-// other CTAs, so they are fetched through the async proxy after the acquiring fences. Lane k owns dims 4k..4k+3.
-template <int G, int NCH>
-__device__ __forceinline__ bool merge_pair(const DecodeParams& p, int first, int nsplit, __half* out_pair,
-                                           float* mbuf, uint64_t* mbar, uint32_t& missued, uint32_t& mwaited,
-                                           const WaitCtx& ctx, int lane) {
-    constexpr int kSplitsPerChunk = kMergeChunk / G;  // a chunk holds whole splits (G divides 16)
-    const float2* mlp = reinterpret_cast<const float2*>(p.ml);
-    const size_t base = (size_t)first * G;
-    const int n = nsplit * G;
-    const int nchunks = (n + kMergeChunk - 1) / kMergeChunk;
-    float M[G], D[G];
-    float4 A[G];
+// Task t of a static plan (split grid or single pass): its row, KV head, split and logical page range. Split tasks
+// are in (b, h, s) order, splits fastest: the CTAs that run at the same time read different page ranges of one head
+// (measured faster on GB300 than eight CTAs reading the eight heads of the same pages).
+struct StaticTask {
+    int b, h, s, pb, pe;
+};
+
+__device__ __forceinline__ StaticTask static_task(const DecodeParams& p, int t) {
+    StaticTask k;
+    if (p.variant == PKV_VARIANT_SPLIT) {
+        const int S = p.num_splits;
+        const int per_row = p.Hkv * S;
+        k.b = t / per_row;
+        const int r = t - k.b * per_row;
+        k.h = r / S;
+        k.s = r - k.h * S;
+        k.pb = k.s * p.chunk_pages;
+        k.pe = k.pb + p.chunk_pages;
+    } else {
+        k.b = t / p.Hkv;
+        k.h = t - k.b * p.Hkv;
+        k.s = 0;
+        k.pb = 0;
+        k.pe = p.max_pages;
+    }
+    return k;
+}
+
+// Pages of a task that lie within its row: the row length is validated (an out-of-range length counts as 0).
+__device__ __forceinline__ int task_pages(const DecodeParams& p, int len, int pb, int pe) {
+    if (len < 0 || len > p.max_pages * kPageSize) len = 0;
+    return max(0, min(pe, (len + kPageSize - 1) / kPageSize) - pb);
+}
+
+// Loader side of a merge task: the pair's S_b * G states (written by other CTAs before their arrivals, which the
+// epilogue warp's counter acquired) go through the ring by bulk copies, kMergeStates states (8 KB of acc) per stage,
+// read through the async proxy. Returns the new ring position, or -1 if a wait gave up.
+template <int G, int NS>
+__device__ __noinline__ int load_merge_chunks(const DecodeParams& p, uint8_t* stages, uint64_t* full, uint64_t* empty,
+                                              int seq, int first, int nsplit, int nchunks, WaitCtx ctx, int lane) {
+    fence_proxy_async_global();
+    const int nstates = nsplit * G;
+    const float* src = p.acc + (size_t)first * G * kHeadDim;
+    for (int c = 0; c < nchunks; ++c) {
+        const int st = seq % NS;
+        if (!warp_wait(&empty[st], ((seq / NS) & 1) ^ 1, ctx)) return -1;
+        if (lane == 0) {
+            const uint32_t bytes = min(kMergeStates, nstates - c * kMergeStates) * kHeadDim * 4;
+            mbar_arrive_expect_tx(&full[st], bytes);
+            bulk_g2s(stages + st * kStageBytes, src + (size_t)c * kMergeStates * kHeadDim, bytes, &full[st]);
+        }
+        __syncwarp();
+        ++seq;
+    }
+    return seq;
+}
+
+// Consumer side of a merge task: warp w folds the states of its stages (chunk i of the task is in stage (seq + i) %
+// NS and belongs to warp (seq + i) % NCW) into a running (M, D, A) per query head (M in base 2; lane k owns dims
+// 4k..4k+3), then hands (M, D) and A to the epilogue warp through the partial-output slot `co` / `cml` once `eempty`
+// allows. The (m, l) pairs come from L2 (those of the warp's first kMlAhead chunks requested at once). Returns
+// false if a wait gave up.
+template <int G, int NS, int NCW>
+__device__ __noinline__ bool fold_merge_chunks(const DecodeParams& p, const uint8_t* stages, uint64_t* full,
+                                               uint64_t* empty, uint64_t* eempty_e, uint32_t eparity, int seq, int w,
+                                               int nchunks, int first, int nsplit, float* co, float2* cml, WaitCtx ctx,
+                                               int lane) {
+    const int nstates = nsplit * G;
+    const float2* mlp = reinterpret_cast<const float2*>(p.ml) + (size_t)first * G;
+    const int i0 = (w - seq % NCW + NCW) % NCW;
+    constexpr int kMlAhead = 8;
+    float2 mlv[kMlAhead];
+#pragma unroll
+    for (int u = 0; u < kMlAhead; ++u) {
+        const int c0 = (i0 + u * NCW) * kMergeStates;
+        mlv[u] = c0 + lane < nstates && lane < kMergeStates ? __ldcg(mlp + c0 + lane) : make_float2(-INFINITY, 0.f);
+    }
+    float Mg[G], Dg[G];
+    float4 Ag[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        M[g] = -INFINITY;
-        D[g] = 0.f;
-        A[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+        Mg[g] = -INFINITY;
+        Dg[g] = 0.f;
+        Ag[g] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    auto issue = [&](int c) {
-        const int cnt = min(kMergeChunk, n - c * kMergeChunk);
-        const uint32_t buf = missued % NCH;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&mbar[buf], cnt * kHeadDim * 4);
-            bulk_g2s(mbuf + buf * kMergeChunk * kHeadDim, p.acc + (base + (size_t)c * kMergeChunk) * kHeadDim,
-                     cnt * kHeadDim * 4, &mbar[buf]);
-        }
-        ++missued;
-    };
-    for (int c = 0; c < min(NCH, nchunks); ++c) issue(c);
-    for (int c = 0; c < nchunks; ++c) {
-        const int cnt = min(kMergeChunk, n - c * kMergeChunk);
-        const float2 ml = lane < cnt ? __ldcg(mlp + base + (size_t)c * kMergeChunk + lane) : make_float2(0.f, 0.f);
-        const uint32_t buf = mwaited % NCH;
-        if (!warp_wait(&mbar[buf], (mwaited / NCH) & 1u, ctx)) return false;
-        ++mwaited;
-        const float* chunk = mbuf + buf * kMergeChunk * kHeadDim;
-        for (int j = 0; j < kSplitsPerChunk && j * G < cnt; ++j) {
+    for (int i = i0, u = 0; i < nchunks; i += NCW, ++u) {
+        const int j = seq + i;
+        const int st = j % NS;
+        const int c0 = i * kMergeStates;
+        const int cnt = min(kMergeStates, nstates - c0);
+        float2 ml = make_float2(-INFINITY, 0.f);
+#pragma unroll
+        for (int v = 0; v < kMlAhead; ++v)
+            if (v == u) ml = mlv[v];
+        if (u >= kMlAhead && lane < cnt) ml = __ldcg(mlp + c0 + lane);
+        if (!warp_wait(&full[st], (j / NS) & 1, ctx)) return false;
+        const float* chunk = reinterpret_cast<const float*>(stages + st * kStageBytes);
+#pragma unroll
+        for (int jj = 0; jj < kMergeStates / G; ++jj) {
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const int lj = j * G + g;
-                const float m2 = __shfl_sync(0xffffffffu, ml.x, lj) * kLog2e;
-                const float l = __shfl_sync(0xffffffffu, ml.y, lj);
-                const float4 v = *reinterpret_cast<const float4*>(chunk + lj * kHeadDim + lane * 4);
-                if (l > 0.f) {
-                    const float mn = fmaxf(M[g], m2);
-                    const float fo = fast_exp2(M[g] - mn), fn = fast_exp2(m2 - mn);
-                    D[g] = D[g] * fo + fn * l;
-                    A[g].x = A[g].x * fo + fn * v.x;
-                    A[g].y = A[g].y * fo + fn * v.y;
-                    A[g].z = A[g].z * fo + fn * v.z;
-                    A[g].w = A[g].w * fo + fn * v.w;
-                    M[g] = mn;
+                const int li = jj * G + g;
+                const float m2 = __shfl_sync(0xffffffffu, ml.x, li) * kLog2e;
+                const float l = __shfl_sync(0xffffffffu, ml.y, li);
+                if (li < cnt && l > 0.f) {
+                    const float4 v = *reinterpret_cast<const float4*>(chunk + li * kHeadDim + lane * 4);
+                    const float mn = fmaxf(Mg[g], m2);
+                    const float fo = fast_exp2(Mg[g] - mn), fn = fast_exp2(m2 - mn);
+                    Dg[g] = Dg[g] * fo + fn * l;
+                    Ag[g].x = Ag[g].x * fo + fn * v.x;
+                    Ag[g].y = Ag[g].y * fo + fn * v.y;
+                    Ag[g].z = Ag[g].z * fo + fn * v.z;
+                    Ag[g].w = Ag[g].w * fo + fn * v.w;
+                    Mg[g] = mn;
                 }
             }
         }
         __syncwarp();
-        if (c + NCH < nchunks) {
-            fence_proxy_async_smem();  // the buffer's generic reads are done before the next copy overwrites it
-            issue(c + NCH);
-        }
+        if (lane == 0) mbar_arrive(&empty[st]);
     }
+    if (!warp_wait(eempty_e, eparity, ctx)) return false;
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-        store_half4(out_pair + (size_t)g * kHeadDim + lane * 4, A[g], D[g] > 0.f ? 1.f / D[g] : 0.f);
+    for (int g = 0; g < G; ++g) {
+        *reinterpret_cast<float4*>(co + g * kCombRow + lane * 4) = Ag[g];
+        if (lane == 0) cml[g] = make_float2(Mg[g], Dg[g]);
+    }
     return true;
 }
 
-// Resident CTAs per SM the kernel is compiled for: two up to G = 4; one for G >= 8, whose partial-output slots do
-// not leave room for a second CTA's shared memory.
-constexpr int ctas_per_sm(int group) { return group >= 8 ? 1 : kDecodeCtasPerSm; }
+// Resident CTAs per SM the kernel is compiled for: two up to G = 8; one for G = 16, whose query rows and
+// partial-output slots do not leave room for a second CTA's shared memory.
+constexpr int ctas_per_sm(int group) { return group >= 16 ? 1 : kDecodeCtasPerSm; }
 
 template <int G, int NCW, int NS, int NTS>
 __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(const __grid_constant__ DecodeParams p) {
@@ -235,13 +309,18 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
     uint64_t* tempty = tq + NTS;      // the slot has been read by the loader and every consumer
     uint64_t* efull = tempty + NTS;   // [2] every consumer warp has written its partial of the task into the slot
     uint64_t* eempty = efull + 2;     // [2] the epilogue warp has read the slot
-    uint64_t* mbar = eempty + 2;      // [kMergeBufs] merge chunk landed
     TaskSlot* slots = reinterpret_cast<TaskSlot*>(smem + L::off_slots);
     EpiHeader* ehdr = reinterpret_cast<EpiHeader*>(smem + L::off_ehdr);
     float* comb_o = reinterpret_cast<float*>(smem + L::off_comb);
     float2* comb_ml = reinterpret_cast<float2*>(smem + L::off_comb_ml);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_flag);
+    volatile int* posted = abort_flag + 1;    // merge requests the epilogue has posted
+    volatile int* taken = abort_flag + 2;     // merge requests the scheduler has published as tasks
+    volatile int* verdicts = abort_flag + 3;  // page tasks the epilogue has finished
+    MergeReq* mreq = reinterpret_cast<MergeReq*>(smem + L::off_mreq);
     const WaitCtx ctx{abort_flag, &p.hdr->status};
+    // the merge of a pair runs as a task of the CTA whose task of the pair arrived last
+    const bool fused = p.fuse_merge != 0 && p.variant != PKV_VARIANT_SINGLE;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
@@ -250,16 +329,46 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
         }
         for (int i = 0; i < NTS; ++i) {
             mbar_init(&tmeta[i], 1);
-            mbar_init(&tq[i], 1);
             mbar_init(&tempty[i], NCW + 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&efull[i], NCW);
             mbar_init(&eempty[i], 1);
         }
-        for (int i = 0; i < L::kMergeBufs; ++i) mbar_init(&mbar[i], 1);
         *abort_flag = 0;
+        *posted = 0;
+        *taken = 0;
+        *verdicts = 0;
         mbar_fence_init();
+    }
+    // Static plans (split grid, single pass; never launched after another grid of this library): the loader and the
+    // scheduler both read the row length and block-table entries of the CTA's first task before the CTA barrier, so
+    // the round trip overlaps the barrier set-up, and the first page copies do not wait for the task slot.
+    int pre_np = 0, pre_h = 0, pre_ent = -1, pre_len = 0;
+    if ((warp == NCW + 1 || warp == NCW + 2) && p.variant != PKV_VARIANT_WORKQUEUE && (int)blockIdx.x < p.num_tasks) {
+        const StaticTask k = static_task(p, blockIdx.x);
+        if (k.b >= 0 && k.b < p.B && k.h >= 0 && k.h < p.Hkv && k.pb >= 0 && k.pe >= k.pb) {
+            const int nent = max(0, min(min(k.pe, p.max_pages) - k.pb, kSlotEntries));
+            pre_ent = lane < nent ? p.block_table[(size_t)k.b * p.max_pages + k.pb + lane] : -1;
+            pre_len = p.seq_lens[k.b];
+            pre_np = min(task_pages(p, pre_len, k.pb, k.pe), nent);
+            pre_h = k.h;
+        }
+    }
+    // The scheduler's lane 0 owns the query barriers; it copies the first static task's query rows into slot 0 right
+    // away, ahead of the loader's first page copies (the consumers wait for them after the CTA barrier).
+    if (warp == NCW + 2 && lane == 0) {
+        for (int i = 0; i < NTS; ++i) mbar_init(&tq[i], 1);
+        mbar_fence_init();
+        if (p.variant != PKV_VARIANT_WORKQUEUE && (int)blockIdx.x < p.num_tasks) {
+            const StaticTask k = static_task(p, blockIdx.x);
+            if (k.b >= 0 && k.b < p.B && k.h >= 0 && k.h < p.Hkv && k.pb >= 0 && k.pe >= k.pb) {
+                mbar_arrive_expect_tx(&tq[0], G * kRowBytes);
+                bulk_g2s(smem + L::off_q,
+                         static_cast<const __half*>(p.q) + ((size_t)k.b * p.Hq + (size_t)k.h * G) * kHeadDim,
+                         G * kRowBytes, &tq[0]);
+            }
+        }
     }
     __syncthreads();
     // A separate merge grid launched after this one waits for its completion before reading anything; it may be
@@ -321,25 +430,97 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
             count = min(*reinterpret_cast<volatile int32_t*>(&p.hdr->task_count), p.task_capacity);
         }
         const __half* q = static_cast<const __half*>(p.q);
-        int tseq = 0;
-        for (int k = 0;; ++k) {
-            int t;
-            if (wq && k > 0) {  // the first wave is static: CTA i starts with task i, no atomic on its critical path
-                int c = 0;
-                if (lane == 0) c = static_cast<int>(gridDim.x + atomicAdd(&p.hdr->queue_head, 1u));
-                t = __shfl_sync(0xffffffffu, c, 0);
+        int tseq = 0;      // slots published
+        int k = 0;         // page tasks claimed
+        int regular = 0;   // page tasks published
+        bool more = true;  // page tasks may remain
+        uint64_t idle_t0 = 0;
+        uint32_t idle_it = 0;
+        for (;;) {
+            // Next slot: a merge the epilogue asked for, else the CTA's next page task; with the merge fused the
+            // end comes only after the epilogue has finished every page task (any of them may still ask for a
+            // merge). The posted count is read after the verdicts, so a request posted before the last verdict
+            // is always seen.
+            int kind, t = 0;
+            // lane 0 reads the mailbox counters (they change under the warp) and the warp follows its decision
+            int pend = 0, idle = 0;  // a request is pending; (fused, no page task left) the epilogue is still busy
+            if (lane == 0 && fused) {
+                if (*posted > *taken) {
+                    pend = 1;
+                } else if (!more) {
+                    const int v = *verdicts;
+                    __threadfence_block();
+                    pend = *posted > *taken;
+                    idle = !pend && v < regular;
+                }
+            }
+            pend = __shfl_sync(0xffffffffu, pend, 0);
+            idle = __shfl_sync(0xffffffffu, idle, 0);
+            if (pend) {
+                kind = kKindMerge;
+            } else if (more) {
+                if (wq && k > 0) {  // the first wave is static: CTA i starts with task i, no atomic on its critical
+                    int c = 0;      // path
+                    if (lane == 0) c = static_cast<int>(gridDim.x + atomicAdd(&p.hdr->queue_head, 1u));
+                    t = __shfl_sync(0xffffffffu, c, 0);
+                } else {
+                    t = blockIdx.x + k * gridDim.x;
+                }
+                ++k;
+                if (t >= count) {
+                    more = false;
+                    continue;
+                }
+                kind = kKindPages;
+            } else if (idle) {  // bounded wait for the epilogue
+                if (++idle_it % kPollEvery == 0) {
+                    const uint64_t now = global_timer_ns();
+                    if (idle_t0 == 0) idle_t0 = now;
+                    const bool stop = (*abort_flag != 0) || (now - idle_t0 > kWaitLimitNs);
+                    if (__any_sync(0xffffffffu, stop)) {
+                        if (lane == 0 && *abort_flag == 0) {
+                            *abort_flag = 1;
+                            raise_status(ctx.status, PKV_STATUS_TIMEOUT);
+                        }
+                        break;
+                    }
+                }
+                __nanosleep(64);
+                continue;
             } else {
-                t = blockIdx.x + k * gridDim.x;
+                kind = -1;
             }
             const int ts = tseq % NTS;
             if (!warp_wait(&tempty[ts], ((tseq / NTS) & 1) ^ 1, ctx)) break;
             TaskSlot* sl = &slots[ts];
-            if (t >= count) {
+            if (kind < 0) {
                 if (lane == 0) {
                     sl->npages = -1;
                     mbar_arrive(&tmeta[ts]);
                 }
                 break;
+            }
+            if (kind == kKindMerge) {
+                if (lane == 0) {
+                    __threadfence_block();  // the entry was written before the posted count
+                    const MergeReq r = mreq[*taken % kMailbox];
+                    *taken = *taken + 1;
+                    sl->b = r.b;
+                    sl->h = r.h;
+                    sl->s = 0;
+                    sl->task = r.first;
+                    sl->page_begin = 0;
+                    sl->npages = (r.nsplit * G + kMergeStates - 1) / kMergeStates;
+                    sl->seq_len = 0;
+                    sl->nsplit = r.nsplit;
+                    sl->kind = kKindMerge;
+                    mbar_arrive(&tq[ts]);  // no query rows
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tmeta[ts]);
+                __syncwarp();
+                ++tseq;
+                continue;
             }
             int b, h, s, pb, pe, task, nsplit = 1;
             if (in_decode) {
@@ -367,26 +548,15 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
                 pb = tk.page_begin;
                 pe = tk.page_end;
                 task = t;
-            } else if (variant == PKV_VARIANT_SPLIT) {
-                // (b, h, s) order, splits fastest: the CTAs that run at the same time read different page ranges of
-                // one head (measured faster on GB300 than eight CTAs reading the eight heads of the same pages)
-                const int S = p.num_splits;
-                const int per_row = Hkv * S;
-                b = t / per_row;
-                const int r = t - b * per_row;
-                h = r / S;
-                s = r - h * S;
-                pb = s * p.chunk_pages;
-                pe = pb + p.chunk_pages;
-                task = t;
-                nsplit = S;
             } else {
-                b = t / Hkv;
-                h = t - b * Hkv;
-                s = 0;
-                pb = 0;
-                pe = p.max_pages;
+                const StaticTask st = static_task(p, t);
+                b = st.b;
+                h = st.h;
+                s = st.s;
+                pb = st.pb;
+                pe = st.pe;
                 task = t;
+                if (variant == PKV_VARIANT_SPLIT) nsplit = p.num_splits;
             }
             const bool bad = b < 0 || b >= p.B || h < 0 || h >= Hkv || s < 0 || pb < 0 || pe < pb;
             if (bad) {  // a task that is not from this plan: it writes a neutral state and takes no part in a merge
@@ -394,17 +564,19 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
                 h = 0;
                 pb = pe = 0;
             }
-            // the row length and the task's first block-table entries, fetched together
+            // the row length and the task's first block-table entries, fetched together (for the CTA's first static
+            // task they were read before the CTA barrier)
+            const bool prefetched = !wq && !bad && t == (int)blockIdx.x;
             const int nent = max(0, min(min(pe, p.max_pages) - pb, kSlotEntries));
-            const int ent = lane < nent ? p.block_table[(size_t)b * p.max_pages + pb + lane] : -1;
-            int len = p.seq_lens[b];
+            const int ent = prefetched ? pre_ent : (lane < nent ? p.block_table[(size_t)b * p.max_pages + pb + lane] : -1);
+            int len = prefetched ? pre_len : p.seq_lens[b];
             const int row_splits = in_decode ? row_S_s[b] : (wq ? p.row_splits[b] : 0);
             if (len < 0 || len > p.max_pages * kPageSize) {
                 if (lane == 0) raise_status(ctx.status, PKV_STATUS_BAD_LEN);
                 len = 0;
             }
             const int np_row = (len + kPageSize - 1) / kPageSize;
-            const int np = max(0, min(pe, np_row) - pb);
+            const int np = task_pages(p, len, pb, pe);
             // A row with pages past its last task (its length grew after the plan was made) is flagged; its tasks
             // still take part in the merge, so the arrival counters stay consistent.
             bool grown, foreign = bad;
@@ -428,22 +600,31 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
                 sl->npages = np;
                 sl->seq_len = len;
                 sl->nsplit = nsplit;
+                sl->kind = kKindPages;
             }
             __syncwarp();
+            // Published before the query copy is issued (that copy may queue behind the loader's page copies). The
+            // G query rows of this KV head are contiguous in q; the consumers wait for them on their own barrier.
+            // The CTA's first static task had its rows copied before the CTA barrier.
             if (lane == 0) {
                 mbar_arrive(&tmeta[ts]);
-                if (np > 0) {  // the G query rows of this KV head are contiguous in q
-                    mbar_arrive_expect_tx(&tq[ts], G * kRowBytes);
-                    bulk_g2s(smem + L::off_q + ts * L::kQRowsBytes, q + ((size_t)b * Hq + (size_t)h * G) * kHeadDim,
-                             G * kRowBytes, &tq[ts]);
-                } else {
-                    mbar_arrive(&tq[ts]);
+                if (!prefetched) {
+                    if (!bad) {
+                        mbar_arrive_expect_tx(&tq[ts], G * kRowBytes);
+                        bulk_g2s(smem + L::off_q + ts * L::kQRowsBytes,
+                                 q + ((size_t)b * Hq + (size_t)h * G) * kHeadDim, G * kRowBytes, &tq[ts]);
+                    } else {
+                        mbar_arrive(&tq[ts]);
+                    }
                 }
             }
             __syncwarp();
             ++tseq;
+            ++regular;
         }
-        // Before the warp leaves, every query copy it issued has landed (only after an abort can one be pending).
+        // Before the warp leaves, every query copy it issued has landed (only after an abort can one be pending),
+        // including the first static task's copy when the warp stopped before publishing its slot.
+        if (tseq == 0 && !wq && (int)blockIdx.x < p.num_tasks) warp_drain(&tq[0], 0);
         for (int j = max(0, tseq - NTS); j < tseq; ++j) warp_drain(&tq[j % NTS], (j / NTS) & 1);
         // Workqueue with the merge fused: rows without tokens have no task, so their (zero) output is written here.
         if (wq && p.fuse_merge) {
@@ -471,15 +652,52 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
         const uint64_t pol = policy_evict_first();
         int seq = 0;
         bool stop = false;
+        // the first pages of the first static task, from the entries read before the CTA barrier (its ring stages
+        // are fresh, so nothing is waited for)
+        const int pre = min(pre_np, NS);
+        for (int i = 0; i < pre; ++i) {
+            const int phys = __shfl_sync(0xffffffffu, pre_ent, i);
+            const bool ok = phys >= 0 && phys < p.num_pages;
+            if (lane == 0) {
+                if (ok) {
+                    uint8_t* dst = smem + L::off_stage + i * kStageBytes;
+                    const int z = phys * kPageSize;
+                    mbar_arrive_expect_tx(&full[i], kStageBytes);
+                    tma_load_3d(dst, &p.tmap_k, 0, pre_h, z, &full[i], pol);
+                    tma_load_3d(dst + kBoxBytes, &p.tmap_k, 64, pre_h, z, &full[i], pol);
+                    tma_load_3d(dst + 2 * kBoxBytes, &p.tmap_v, 0, pre_h, z, &full[i], pol);
+                    tma_load_3d(dst + 3 * kBoxBytes, &p.tmap_v, 64, pre_h, z, &full[i], pol);
+                } else {
+                    raise_status(ctx.status, PKV_STATUS_BAD_PAGE);
+                    mbar_arrive(&full[i]);
+                }
+            }
+        }
+        seq = pre;
         for (int tseq = 0; !stop; ++tseq) {
             const int ts = tseq % NTS;
             if (!warp_wait(&tmeta[ts], (tseq / NTS) & 1, ctx)) break;
             const int np = slots[ts].npages;
             const int b = slots[ts].b, h = slots[ts].h, pb = slots[ts].page_begin;
+            const int kind = slots[ts].kind, mfirst = slots[ts].task, mnsplit = slots[ts].nsplit;
             int ent = slots[ts].ent[lane];
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[ts]);
             if (np < 0) break;
+            if (kind == kKindMerge) {
+                seq = load_merge_chunks<G, NS>(p, smem + L::off_stage, full, empty, seq, mfirst, mnsplit, np, ctx,
+                                               lane);
+                if (seq < 0) break;
+                continue;
+            }
+            const int skip = tseq == 0 ? pre : 0;  // pages issued before the slot was read
+            if (np < skip || (skip > 0 && h != pre_h)) {  // the slot disagrees with the prefetch: never expected
+                if (lane == 0) {
+                    raise_status(ctx.status, PKV_STATUS_TASKS);
+                    *abort_flag = 1;
+                }
+                break;
+            }
             const int32_t* bt = p.block_table + (size_t)b * p.max_pages + pb;
             int ent_next = kSlotEntries + lane < np ? bt[kSlotEntries + lane] : 0;
             for (int c0 = 0; c0 < np; c0 += 32) {
@@ -488,7 +706,7 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
                     if (c0 + 32 + lane < np) ent_next = bt[c0 + 32 + lane];
                 }
                 const int n = min(32, np - c0);
-                for (int i = 0; i < n; ++i) {
+                for (int i = c0 == 0 ? skip : 0; i < n; ++i) {
                     const int phys = __shfl_sync(0xffffffffu, ent, i);
                     const bool ok = phys >= 0 && phys < p.num_pages;
                     if (!ok && lane == 0) raise_status(ctx.status, PKV_STATUS_BAD_PAGE);
@@ -520,14 +738,12 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
         for (int j = max(0, seq - NS); j < seq; ++j) warp_drain(&full[j % NS], (j / NS) & 1);
     } else if (warp == NCW) {
         // ------------------------------------------------------------------ epilogue
-        const bool fused = p.fuse_merge != 0 && p.variant != PKV_VARIANT_SINGLE;
-        float* mbuf = reinterpret_cast<float*>(smem + L::off_mbuf);
-        uint32_t missued = 0, mwaited = 0;
         for (int tseq = 0;; ++tseq) {
             const int e = tseq & 1;
             if (!warp_wait(&efull[e], (tseq >> 1) & 1, ctx)) break;
             const EpiHeader hd = ehdr[e];
             if (hd.npages < 0) break;
+            const bool merge = hd.kind == kKindMerge;
             const float* co = comb_o + e * L::kCombFloats;
             const float2* cml = comb_ml + e * NCW * G;
             for (int g = 0; g < G; ++g) {
@@ -549,7 +765,7 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
                         a.w += f * v.w;
                     }
                 }
-                if (p.variant == PKV_VARIANT_SINGLE) {
+                if (p.variant == PKV_VARIANT_SINGLE || merge) {  // out = acc / l of the whole row
                     store_half4(static_cast<__half*>(p.out) + ((size_t)hd.b * Hq + hd.h * G + g) * kHeadDim + lane * 4,
                                 a, lsum > 0.f ? 1.f / lsum : 0.f);
                 } else {
@@ -562,30 +778,41 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&eempty[e]);  // the consumers may refill the slot
-            if (fused) {
-                // count the task in (b, h); the last arriver merges all S_b states of the pair
+            if (fused && !merge) {
+                // count the task in (b, h); the last arriver asks for the merge of the pair's S_b states
                 fence_acq_rel_gpu();  // this lane's state stores are performed before the arrival
                 __syncwarp();
-                int last = 0;
-                if (lane == 0 && hd.nsplit > 0) {
+                if (lane == 0) {
                     uint32_t* cnt = p.counters + (size_t)hd.b * Hkv + hd.h;
-                    const uint32_t old = atomicAdd(cnt, 1u);
-                    last = old + 1u == (uint32_t)hd.nsplit;
-                    if (last) atomicExch(cnt, 0u);  // re-armed for the next step
+                    bool last = false;
+                    if (hd.nsplit > 0) {
+                        const uint32_t old = atomicAdd(cnt, 1u);
+                        last = old + 1u == (uint32_t)hd.nsplit;
+                        if (last) {
+                            fence_acq_rel_gpu();  // the other tasks' states, published before their arrivals
+                            const int n = *posted;
+                            if (n - *taken >= kMailbox) {  // never expected: requests are taken one per slot
+                                raise_status(ctx.status, PKV_STATUS_TASKS);
+                                *abort_flag = 1;
+                            } else {
+                                MergeReq r;
+                                r.b = hd.b;
+                                r.h = hd.h;
+                                r.first = hd.task - hd.s;
+                                r.nsplit = hd.nsplit;
+                                mreq[n % kMailbox] = r;
+                                __threadfence_block();
+                                *posted = n + 1;
+                            }
+                        }
+                    }
+                    __threadfence_block();  // a request is posted before the verdict that lets the scheduler end
+                    *verdicts = *verdicts + 1;
+                    if (last) atomicExch(cnt, 0u);  // re-armed for the next step (off the merge's critical path)
                 }
-                last = __shfl_sync(0xffffffffu, last, 0);
-                if (last) {
-                    fence_acq_rel_gpu();         // the other tasks' states, published before their arrivals ...
-                    fence_proxy_async_global();  // ... are visible to the bulk copies that read them
-                    if (!merge_pair<G, L::kMergeBufs>(p, hd.task - hd.s, hd.nsplit,
-                                       static_cast<__half*>(p.out) + ((size_t)hd.b * Hq + (size_t)hd.h * G) * kHeadDim,
-                                       mbuf, mbar, missued, mwaited, ctx, lane))
-                        break;
-                }
+                __syncwarp();
             }
         }
-        // Wait for the merge chunks still in flight (only after an abort can one be pending).
-        for (uint32_t j = mwaited; j < missued; ++j) warp_drain(&mbar[j % L::kMergeBufs], (j / L::kMergeBufs) & 1u);
     } else {
         // ------------------------------------------------------------------ consumers
         const int w = warp;
@@ -619,6 +846,32 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
             const int sb = slots[ts].b, sh = slots[ts].h, ss = slots[ts].s, stask = slots[ts].task;
             const int spb = slots[ts].page_begin, slen = slots[ts].seq_len, snsplit = slots[ts].nsplit;
             if (!warp_wait(&tq[ts], (tseq / NTS) & 1, ctx)) break;
+            if (slots[ts].kind == kKindMerge) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[ts]);
+                // Merge task: the fold of this warp's stages and its hand-off to the epilogue warp.
+                if (!fold_merge_chunks<G, NS, NCW>(p, smem + L::off_stage, full, empty, &eempty[e],
+                                                   ((tseq >> 1) & 1) ^ 1, seq, w, npages, stask, snsplit,
+                                                   comb_o + e * L::kCombFloats + w * G * kCombRow,
+                                                   comb_ml + e * NCW * G + w * G, ctx, lane))
+                    break;
+                seq += npages;
+                if (w == 0 && lane == 0) {
+                    EpiHeader hd;
+                    hd.b = sb;
+                    hd.h = sh;
+                    hd.s = 0;
+                    hd.task = stask;
+                    hd.nsplit = snsplit;
+                    hd.npages = npages;
+                    hd.kind = kKindMerge;
+                    hd.pad = 0;
+                    ehdr[e] = hd;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&efull[e]);
+                continue;
+            }
             // Q^T as the B operand: b0 = Q[head][16ks + 2t, +1], b1 = Q[head][16ks + 2t + 8, +9], head = 8nt + g
             uint32_t qb[8][kNT][2];
             {
@@ -800,7 +1053,8 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
                 hd.task = stask;
                 hd.nsplit = snsplit;
                 hd.npages = npages;
-                hd.pad0 = hd.pad1 = 0;
+                hd.kind = kKindPages;
+                hd.pad = 0;
                 ehdr[e] = hd;
             }
             __syncwarp();
