@@ -186,6 +186,56 @@ __device__ __forceinline__ StaticTask static_task(const DecodeParams& p, int t) 
     return k;
 }
 
+// The CTA's first task (task blockIdx.x) when it can be known before the CTA barrier: for a static plan from the
+// task index, for a workqueue whose compact list the decode derives itself from seq_lens (a warp-collective scan
+// of Hkv * S_b over the rows, the arithmetic of the list derivation below). Plans that run a list written by the
+// worklist builder are launched after it and read nothing before griddepcontrol.wait: no first task here. Returns
+// false when there is no such task.
+__device__ __forceinline__ bool first_task(const DecodeParams& p, int lane, StaticTask& k, int& len) {
+    const int t = blockIdx.x;
+    if (p.variant != PKV_VARIANT_WORKQUEUE) {
+        if (t >= p.num_tasks) return false;
+        k = static_task(p, t);
+        if (!(k.b >= 0 && k.b < p.B && k.h >= 0 && k.h < p.Hkv && k.pb >= 0 && k.pe >= k.pb)) return false;
+        len = p.seq_lens[k.b];
+        return true;
+    }
+    if (!p.list_in_decode || p.B > PKV_MAX_ROWS_IN_DECODE) return false;
+    int run = 0, found = -1, fl = 0, foff = 0, fS = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const int b = b0 + lane;
+        int l = b < p.B ? p.seq_lens[b] : 0;
+        if (l < 0 || l > p.max_pages * kPageSize) l = 0;
+        const int S = ((l + kPageSize - 1) / kPageSize + p.chunk_pages - 1) / p.chunk_pages;
+        const int x = b < p.B ? p.Hkv * S : 0;
+        int incl = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int off = run + incl - x;
+        const unsigned hit = __ballot_sync(0xffffffffu, x > 0 && off <= t && t < off + x);
+        if (found < 0 && hit) {
+            const int src = __ffs(hit) - 1;
+            found = b0 + src;
+            fl = __shfl_sync(0xffffffffu, l, src);
+            foff = __shfl_sync(0xffffffffu, off, src);
+            fS = __shfl_sync(0xffffffffu, S, src);
+        }
+        run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (found < 0 || t >= min(run, p.task_capacity)) return false;
+    const int r = t - foff;
+    k.b = found;
+    k.h = r / fS;
+    k.s = r - k.h * fS;
+    k.pb = k.s * p.chunk_pages;
+    k.pe = min(k.pb + p.chunk_pages, (fl + kPageSize - 1) / kPageSize);
+    len = fl;
+    return true;
+}
+
 // Pages of a task that lie within its row: the row length is validated (an out-of-range length counts as 0).
 __device__ __forceinline__ int task_pages(const DecodeParams& p, int len, int pb, int pe) {
     if (len < 0 || len > p.max_pages * kPageSize) len = 0;
@@ -341,33 +391,32 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
         *verdicts = 0;
         mbar_fence_init();
     }
-    // Static plans (split grid, single pass; never launched after another grid of this library): the loader and the
-    // scheduler both read the row length and block-table entries of the CTA's first task before the CTA barrier, so
-    // the round trip overlaps the barrier set-up, and the first page copies do not wait for the task slot.
+    // The loader and the scheduler both work out the CTA's first task before the CTA barrier (first_task): the
+    // scheduler's lane 0, which owns the query barriers, copies its query rows into slot 0 at once, and both read
+    // its row length and block-table entries, so the loader's first page copies wait neither for the barrier set-up
+    // nor for the task slot.
     int pre_np = 0, pre_h = 0, pre_ent = -1, pre_len = 0;
-    if ((warp == NCW + 1 || warp == NCW + 2) && p.variant != PKV_VARIANT_WORKQUEUE && (int)blockIdx.x < p.num_tasks) {
-        const StaticTask k = static_task(p, blockIdx.x);
-        if (k.b >= 0 && k.b < p.B && k.h >= 0 && k.h < p.Hkv && k.pb >= 0 && k.pe >= k.pb) {
-            const int nent = max(0, min(min(k.pe, p.max_pages) - k.pb, kSlotEntries));
-            pre_ent = lane < nent ? p.block_table[(size_t)k.b * p.max_pages + k.pb + lane] : -1;
-            pre_len = p.seq_lens[k.b];
-            pre_np = min(task_pages(p, pre_len, k.pb, k.pe), nent);
-            pre_h = k.h;
-        }
-    }
-    // The scheduler's lane 0 owns the query barriers; it copies the first static task's query rows into slot 0 right
-    // away, ahead of the loader's first page copies (the consumers wait for them after the CTA barrier).
-    if (warp == NCW + 2 && lane == 0) {
-        for (int i = 0; i < NTS; ++i) mbar_init(&tq[i], 1);
-        mbar_fence_init();
-        if (p.variant != PKV_VARIANT_WORKQUEUE && (int)blockIdx.x < p.num_tasks) {
-            const StaticTask k = static_task(p, blockIdx.x);
-            if (k.b >= 0 && k.b < p.B && k.h >= 0 && k.h < p.Hkv && k.pb >= 0 && k.pe >= k.pb) {
+    bool pre_ok = false;
+    if (warp == NCW + 1 || warp == NCW + 2) {
+        StaticTask k;
+        int len = 0;
+        pre_ok = first_task(p, lane, k, len);
+        if (warp == NCW + 2 && lane == 0) {
+            for (int i = 0; i < NTS; ++i) mbar_init(&tq[i], 1);
+            mbar_fence_init();
+            if (pre_ok) {
                 mbar_arrive_expect_tx(&tq[0], G * kRowBytes);
                 bulk_g2s(smem + L::off_q,
                          static_cast<const __half*>(p.q) + ((size_t)k.b * p.Hq + (size_t)k.h * G) * kHeadDim,
                          G * kRowBytes, &tq[0]);
             }
+        }
+        if (pre_ok) {
+            const int nent = max(0, min(min(k.pe, p.max_pages) - k.pb, kSlotEntries));
+            pre_ent = lane < nent ? p.block_table[(size_t)k.b * p.max_pages + k.pb + lane] : -1;
+            pre_len = len;
+            pre_np = min(task_pages(p, pre_len, k.pb, k.pe), nent);
+            pre_h = k.h;
         }
     }
     __syncthreads();
@@ -442,6 +491,7 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
             // merge). The posted count is read after the verdicts, so a request posted before the last verdict
             // is always seen.
             int kind, t = 0;
+            bool first = false;  // the CTA's first task (task blockIdx.x), worked out before the CTA barrier
             // lane 0 reads the mailbox counters (they change under the warp) and the warp follows its decision
             int pend = 0, idle = 0;  // a request is pending; (fused, no page task left) the epilogue is still busy
             if (lane == 0 && fused) {
@@ -466,6 +516,7 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
                 } else {
                     t = blockIdx.x + k * gridDim.x;
                 }
+                first = k == 0;
                 ++k;
                 if (t >= count) {
                     more = false;
@@ -566,7 +617,7 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
             }
             // the row length and the task's first block-table entries, fetched together (for the CTA's first static
             // task they were read before the CTA barrier)
-            const bool prefetched = !wq && !bad && t == (int)blockIdx.x;
+            const bool prefetched = first && pre_ok && !bad;
             const int nent = max(0, min(min(pe, p.max_pages) - pb, kSlotEntries));
             const int ent = prefetched ? pre_ent : (lane < nent ? p.block_table[(size_t)b * p.max_pages + pb + lane] : -1);
             int len = prefetched ? pre_len : p.seq_lens[b];
@@ -623,8 +674,8 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
             ++regular;
         }
         // Before the warp leaves, every query copy it issued has landed (only after an abort can one be pending),
-        // including the first static task's copy when the warp stopped before publishing its slot.
-        if (tseq == 0 && !wq && (int)blockIdx.x < p.num_tasks) warp_drain(&tq[0], 0);
+        // including the first task's copy when the warp stopped before publishing its slot.
+        if (tseq == 0 && pre_ok) warp_drain(&tq[0], 0);
         for (int j = max(0, tseq - NTS); j < tseq; ++j) warp_drain(&tq[j % NTS], (j / NTS) & 1);
         // Workqueue with the merge fused: rows without tokens have no task, so their (zero) output is written here.
         if (wq && p.fuse_merge) {
