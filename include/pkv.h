@@ -87,8 +87,10 @@ typedef struct pkv_problem {
  * roofline-style policy", the gist.science technical summary's "Calibrated Adaptive Policy"). For a candidate plan
  * with T tasks on W resident CTAs, A = min(T, W) of them busy, kv = the step's K/V bytes and task bytes = c pages of
  * one KV head's K and V:
- *   workqueue (dynamic):   decode = launch_us + kv / min(hbm_gbs, A * wq_cta_gbs) + (T / W) * task_us
- *                                   + tail * task_bytes / wq_cta_gbs
+ *   workqueue (dynamic):   stream = kv / min(hbm_gbs, A * wq_cta_gbs)
+ *                          decode = launch_us + stream + (T / W) * task_us
+ *                                   + tail * max(0, ceil(T / W) * task_bytes / wq_cta_gbs - stream)
+ *                          (the last term: the CTAs that run ceil(T / W) tasks at their own rate outlast the stream)
  *   split, single (static): decode = launch_us + ceil(T / W) * (task_us + (kv / T) / min(cta_gbs, hbm_gbs / A))
  *   merge  = merge_us + merge_state_us * S_max              separate merge kernel (launched with PDL)
  *          | fused_us + fused_state_us * S_max * G          merge fused into the last task of each (row, KV head)
@@ -104,7 +106,7 @@ typedef struct pkv_policy {
     double cta_gbs;         /* KV streaming bandwidth of one CTA of the static grid (split, single) */
     double wq_cta_gbs;      /* KV streaming bandwidth of one CTA pulling from the workqueue */
     double task_us;         /* per-task cost on one CTA (scheduling, q, epilogue) */
-    double tail;            /* workqueue: share of one task's time left over after the queue drains */
+    double tail;            /* workqueue: weight of the per-CTA makespan beyond the bandwidth-bound stream */
     double merge_us;        /* separate merge: cost it adds to the step */
     double merge_state_us;  /* separate merge: per split of the longest (row, KV head) */
     double fused_us;        /* fused merge: cost of the last arrival and its merge */
@@ -126,8 +128,9 @@ typedef struct pkv_plan_t {
     int32_t grid_ctas;   /* persistent decode grid size (resident CTAs, at most one wave) */
     int32_t group;       /* G = Hq / Hkv */
     int32_t num_sms;     /* SM count the plan was made for */
-    int32_t fuse_merge;  /* split / workqueue: 1 = pkv_decode merges the split states itself (the last task of every
-                            (row, KV head) to finish merges them and writes out; pkv_merge is then a no-op);
+    int32_t fuse_merge;  /* split / workqueue: 1 = pkv_decode merges the split states itself (the CTA whose task of
+                            a (row, KV head) finishes last runs the pair's merge as one more task: its states go
+                            through that CTA's page ring, and it writes out; pkv_merge is then a no-op);
                             0 = pkv_decode writes partial states only and pkv_merge combines them. The planners set
                             1; a caller may set 0 (the workspace layout does not depend on it). */
     int32_t list_in_decode; /* workqueue: 1 = the decode kernel derives the compact list itself from seq_lens (every
@@ -219,7 +222,8 @@ int pkv_build_worklist(const pkv_plan_t* plan, const pkv_problem* problem, const
  *   single: one task per (row, KV head); writes the normalised output to out.
  *   split / workqueue: one task per (row, KV head, split) writes the partial (m, l, acc) state of its G query heads
  *     into the workspace (empty rectangular splits write m = -inf, l = 0, acc = 0). With plan->fuse_merge = 1 the
- *     last task of each (row, KV head) also merges that pair's states and writes out; with 0, follow with pkv_merge.
+ *     CTA that finishes the last task of each (row, KV head) also merges that pair's states and writes out; with 0,
+ *     follow with pkv_merge.
  *   workqueue: with plan->list_in_decode = 0 runs the list the last pkv_build_worklist wrote into ws (call it first,
  *     on the same stream); with 1 derives the same list from seq_lens_dev itself.
  * scale multiplies q.k (use 1/sqrt(head_dim)). out may be NULL only for split / workqueue plans with fuse_merge 0.

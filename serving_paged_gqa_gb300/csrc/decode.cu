@@ -703,8 +703,8 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
         const uint64_t pol = policy_evict_first();
         int seq = 0;
         bool stop = false;
-        // the first pages of the first static task, from the entries read before the CTA barrier (its ring stages
-        // are fresh, so nothing is waited for)
+        // the first pages of the CTA's first task, from the entries read before the CTA barrier (its ring stages are
+        // fresh, so nothing is waited for)
         const int pre = min(pre_np, NS);
         for (int i = 0; i < pre; ++i) {
             const int phys = __shfl_sync(0xffffffffu, pre_ent, i);

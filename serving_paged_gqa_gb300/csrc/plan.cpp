@@ -155,8 +155,9 @@ double predict_us(const pkv_policy* pol, const pkv_plan_t* plan, const int32_t* 
     const double gb = 1e3;  // bytes / (GB/s * 1e3) = microseconds
     double t;
     if (plan->variant == PKV_VARIANT_WORKQUEUE) {
-        t = pol->launch_us + plan->kv_bytes / (std::min(pol->hbm_gbs, A * pol->wq_cta_gbs) * gb) +
-            (T / W) * pol->task_us + pol->tail * task_bytes / (pol->wq_cta_gbs * gb);
+        const double stream = plan->kv_bytes / (std::min(pol->hbm_gbs, A * pol->wq_cta_gbs) * gb);
+        const double makespan = std::ceil(T / W) * task_bytes / (pol->wq_cta_gbs * gb);
+        t = pol->launch_us + stream + (T / W) * pol->task_us + pol->tail * std::max(0.0, makespan - stream);
     } else {
         const double share = std::min(pol->cta_gbs, pol->hbm_gbs / A) * gb;
         t = pol->launch_us + std::ceil(T / W) * (pol->task_us + (plan->kv_bytes / T) / share);
