@@ -316,20 +316,20 @@ def time_workload(pkv, torch, wl, K, W, args, sms, dev, flush, stream):
     step_ms = np.array([e[0].elapsed_time(e[3]) for e in ev])
     ev = timed_pass(True)
     status = pkv.pkv_read_status(ws)
-    read_ms = read_floor(torch, dev, stream, flush, [plans[j].kv_bytes for j in idx], spin_cycles)
+    copy_ms = copy_same_bytes(torch, dev, stream, flush, [plans[j].kv_bytes for j in idx], spin_cycles)
     dec_ms = np.array([e[1].elapsed_time(e[2]) for e in ev])
     merge_ms = np.array([e[2].elapsed_time(e[3]) for e in ev])  # zero-length pair unless the merge is separate
     build_ms = np.array([e[0].elapsed_time(e[1]) for e in ev])
     kv_bytes = np.array([plans[j].kv_bytes for j in idx])
     return {"idx": idx, "plans": [plans[j] for j in idx], "step_ms": step_ms, "dec_ms": dec_ms, "merge_ms": merge_ms,
-            "build_ms": build_ms, "read_ms": read_ms,
+            "build_ms": build_ms, "copy_ms": copy_ms,
             "kv_bytes": kv_bytes, "launches": launches, "status": status, "ws": ws, "out": out}
 
 
-def read_floor(torch, dev, stream, flush, sizes, spin_cycles):
-    """The same protocol (L2 flushed, GPU spin, CUDA events) around one device-to-device copy that moves each step's
-    algorithmic bytes (half read, half written: the measured HBM peak is such a copy): what one launch moving those
-    bytes takes on this part, launch and event costs included."""
+def copy_same_bytes(torch, dev, stream, flush, sizes, spin_cycles):
+    """The same protocol (L2 flushed, GPU spin, CUDA events) around one device-to-device torch copy that moves each
+    step's algorithmic bytes (half read, half written), the operation the measured HBM peak is taken with: what moving
+    those bytes in one call takes on this part at this size, launch and event costs included."""
     half = int(max(sizes)) // 2 + 256
     src = torch.zeros(half, dtype=torch.uint8, device=dev)
     dst = torch.empty(half, dtype=torch.uint8, device=dev)
@@ -356,7 +356,7 @@ def by_tokens(wl, r):
         groups.setdefault(key, []).append(k)
     return {key: {"steps": len(ks), "step_us": 1e3 * float(r["step_ms"][ks].mean()),
                   "decode_us": 1e3 * float(r["dec_ms"][ks].mean()),
-                  "read_floor_us": 1e3 * float(r["read_ms"][ks].mean()),
+                  "copy_same_bytes_us": 1e3 * float(r["copy_ms"][ks].mean()),
                   "bytes": float(r["kv_bytes"][ks].mean())} for key, ks in sorted(groups.items(), key=lambda x: int(x[0]))}
 
 
@@ -368,9 +368,9 @@ def summarize(pkv, wl, r, peak):
             "decode_us_mean": 1e3 * float(r["dec_ms"].mean()),
             "merge_us_mean": 1e3 * float(r["merge_ms"].mean()), "build_us_mean": 1e3 * float(r["build_ms"].mean()),
             "decode_frac": float(r["kv_bytes"].sum() / (r["dec_ms"].sum() * 1e-3)) / 1e9 / peak,
-            "read_floor_us_mean": 1e3 * float(r["read_ms"].mean()),
-            "read_floor_frac": float(r["kv_bytes"].sum() / (r["read_ms"].sum() * 1e-3)) / 1e9 / peak,
-            "decode_vs_read_floor": float(r["read_ms"].sum() / r["dec_ms"].sum()),
+            "copy_same_bytes_us_mean": 1e3 * float(r["copy_ms"].mean()),
+            "copy_same_bytes_frac": float(r["kv_bytes"].sum() / (r["copy_ms"].sum() * 1e-3)) / 1e9 / peak,
+            "copy_over_decode_time": float(r["copy_ms"].sum() / r["dec_ms"].sum()),
             "step_frac": float(r["kv_bytes"].sum() / (r["step_ms"].sum() * 1e-3)) / 1e9 / peak,
             "algorithmic_bytes_per_step": float(r["kv_bytes"].mean()),
             "variants_used": sorted({pkv.VARIANT_NAMES[p.variant] for p in plans}),
@@ -746,10 +746,11 @@ def run_ours(args):
         "decode_us_mean": head["decode_us_mean"], "step_us_mean": head["step_us_mean"],
         "merge_us_mean": head["merge_us_mean"], "build_us_mean": head["build_us_mean"],
         "step_frac": head["step_frac"], "launches_per_step": head["launches_per_step"], "by_tokens": head["by_tokens"],
-        "read_floor": {"us_mean": head["read_floor_us_mean"], "frac": head["read_floor_frac"],
-                       "decode_vs_read_floor": head["decode_vs_read_floor"],
-                       "what": "one device-to-device copy moving each timed step's algorithmic bytes (half read, "
-                               "half written, as the measured peak), same flush / spin / event protocol"},
+        "copy_same_bytes": {"us_mean": head["copy_same_bytes_us_mean"], "frac": head["copy_same_bytes_frac"],
+                            "copy_over_decode_time": head["copy_over_decode_time"],
+                            "what": "one device-to-device torch copy moving each timed step's algorithmic bytes "
+                                    "(half read, half written, as the measured peak), same flush / spin / event "
+                                    "protocol"},
         "wall_us_per_step": wall_us, "wall_tokens_per_s": None if wall_us is None else B / (wall_us * 1e-6),
         "timed_wall_s": timed_wall, "gpu_launches": r["launches"], "device_status": int(r["status"]),
         "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
