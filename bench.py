@@ -455,65 +455,59 @@ def run_reference(args):
 
 # ------------------------------------------------------------------------------------------------ our arm
 def run_e2e(pkv, torch, wl, idx, args, sms, flush, stream, dev):
-    """The same steps through the public API from pinned host buffers, host wall clock with a synchronize on both
-    sides: one H2D copy of (q, block table, lengths, new K, new V), pkv_plan + pkv_decode_step_append (the new
-    token's K/V written into its page slot inside the decode), one D2H copy of out."""
+    """The same steps through the public serving call, host wall clock with a synchronize on both sides: each step's
+    inputs (q, the new token's K/V, block table, lengths) sit packed in pinned host memory (pkv_step_input_layout);
+    one pkv_serve_step call plans the step from the host lengths, copies the packed input to the device, runs the
+    decode with the new token's K/V appended into its page slot, and copies out back to pinned host memory; then the
+    stream is synchronised. The call's arguments are marshalled once per step buffer (ServeStep), as a server keeps
+    its per-layer buffers."""
     B, Hq, Hkv, d, ps = wl.B, wl.Hq, wl.Hkv, wl.d, wl.ps
     scale = 1.0 / math.sqrt(d)
-    recs = []
-    for j in idx:
-        s = wl.steps[j]
-        tr = wl.traces[s["trace"]][0]
-        lens = s["lens_host"]
-        new_phys = s["bt_host"][np.arange(B), (lens - 1) // ps]
-        new_slot = (lens - 1) % ps
-        used_index = {int(p): i for i, p in enumerate(tr.used_pages)}
-        k_new = np.stack([tr.k_pages[used_index[int(new_phys[b])], int(new_slot[b])] for b in range(B)])
-        v_new = np.stack([tr.v_pages[used_index[int(new_phys[b])], int(new_slot[b])] for b in range(B)])
-        parts = [s["q_host"].view(np.uint8).ravel(), k_new.view(np.uint8).ravel(), v_new.view(np.uint8).ravel(),
-                 s["bt_host"].view(np.uint8).ravel(), lens.view(np.uint8).ravel()]
-        # one pinned buffer, every part starting on a 256-byte boundary (the library wants 16-byte aligned q)
-        sizes = [-(-p.size // 256) * 256 for p in parts]
-        buf = np.zeros(sum(sizes), dtype=np.uint8)
-        o = np.cumsum([0] + sizes)
-        for i, part in enumerate(parts):
-            buf[o[i]:o[i] + part.size] = part
-        packed = torch.from_numpy(buf).pin_memory()
-        recs.append((j, packed, [p.size for p in parts], o))
-    nbytes_max = max(p.numel() for _, p, _, _ in recs)
-    dbuf = torch.empty(nbytes_max, dtype=torch.uint8, device=dev)
     out_d = torch.empty((B, Hq, d), dtype=torch.float16, device=dev)
     out_h = torch.empty((B, Hq, d), dtype=torch.float16).pin_memory()
     # the workspace is allocated once, before the timed steps, for the largest plan among them
     ws_bytes = max(make_plan(pkv, wl.problem(pkv, wl.steps[j]["trace"]), wl.steps[j]["lens_host"], sms, args).ws_bytes
                    for j in idx)
     ws = pkv.alloc_workspace(ws_bytes, dev)
-    times = []
-    h2d = d2h = 0
-    for j, packed, sizes, o in recs:
+    totals = [pkv.pkv_step_input_layout(wl.problem(pkv, wl.steps[j]["trace"]))[1] for j in idx]
+    dev_in = torch.empty(max(totals), dtype=torch.uint8, device=dev)
+    policy = None
+    if args.variant != "auto" or args.separate_merge:
+        return None  # the serving call runs the policy's plans only
+    runners = []
+    for j in idx:
         s = wl.steps[j]
         tr, kpool, vpool = wl.traces[s["trace"]]
         problem = wl.problem(pkv, s["trace"])
+        lens = s["lens_host"]
+        new_phys = s["bt_host"][np.arange(B), (lens - 1) // ps]
+        new_slot = (lens - 1) % ps
+        used_index = {int(p): i for i, p in enumerate(tr.used_pages)}
+        k_new = np.stack([tr.k_pages[used_index[int(new_phys[b])], int(new_slot[b])] for b in range(B)])
+        v_new = np.stack([tr.v_pages[used_index[int(new_phys[b])], int(new_slot[b])] for b in range(B)])
+        offs, total = pkv.pkv_step_input_layout(problem)
+        buf = np.zeros(total, dtype=np.uint8)
+        for o, part in zip(offs, (s["q_host"], k_new, v_new, s["bt_host"], lens)):
+            raw = np.ascontiguousarray(part).view(np.uint8).ravel()
+            buf[o:o + raw.size] = raw
+        host_in = torch.from_numpy(buf).pin_memory()
+        runners.append((pkv.ServeStep(problem, host_in, dev_in, kpool, vpool, scale, ws, out_d, out_h, stream,
+                                      policy, sms), total))
+    times = []
+    h2d = d2h = 0
+    for runner, total in runners:
         flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        dbuf[:packed.numel()].copy_(packed, non_blocking=True)
-        part = [dbuf[o[i]:o[i] + sizes[i]] for i in range(5)]
-        q = part[0].view(torch.float16).view(B, Hq, d)
-        k_new = part[1].view(torch.float16).view(B, Hkv, d)
-        v_new = part[2].view(torch.float16).view(B, Hkv, d)
-        bt = part[3].view(torch.int32).view(B, tr.max_pages)
-        lens = part[4].view(torch.int32)
-        plan = make_plan(pkv, problem, s["lens_host"], sms, args)
-        pkv.pkv_decode_step_append(plan, problem, q, k_new, v_new, kpool, vpool, bt, lens, scale, ws, out_d, stream)
-        out_h.copy_(out_d, non_blocking=True)
-        torch.cuda.current_stream(dev).synchronize()
+        runner.run()
+        stream.synchronize()
         times.append(time.perf_counter() - t0)
-        h2d = packed.numel()
+        h2d = total
         d2h = out_h.numel() * 2
     return {"value": B * len(times) / float(np.sum(times)), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": len(times), "us_per_step": 1e6 * float(np.mean(times)),
-            "timing": "host wall clock per step, synchronize on both sides; includes pkv_plan"}
+            "timing": "host wall clock per step, synchronize on both sides; one pkv_serve_step call: pkv_plan on the "
+                      "host lengths, H2D of the packed input, decode with the KV append fused, D2H of out"}
 
 
 def run_multilayer(pkv, torch, args, sms, dev, stream, peak, name="b8_bimodal", seed=5, layers=8):

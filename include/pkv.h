@@ -263,6 +263,30 @@ int pkv_decode_step_append(const pkv_plan_t* plan, const pkv_problem* problem, c
                            const int32_t* seq_lens_dev, float scale, void* ws, size_t ws_bytes, void* out,
                            void* stream);
 
+/*
+ * Byte offsets of the five parts of a packed step input (pkv_serve_step): offsets[0] q [B][Hq][d] fp16, [1] k_new
+ * [B][Hkv][d] fp16, [2] v_new [B][Hkv][d] fp16, [3] block_table [B][max_pages_per_seq] int32, [4] seq_lens [B]
+ * int32 (counting the new token), each part starting on a 256-byte boundary; *total = the buffer's size in bytes.
+ * Host only. Returns PKV_OK, PKV_E_NULLPTR or a pkv_check_problem error.
+ */
+int pkv_step_input_layout(const pkv_problem* problem, size_t offsets[5], size_t* total);
+
+/*
+ * One serving step of a layer from host memory in a single call: plans the step (pkv_plan with `policy`, NULL = the
+ * built-in constants, on the seq_lens of host_in, which the CPU reads during the call), then enqueues on `stream` the
+ * copy of the packed input host_in (layout of pkv_step_input_layout; pinned host memory for an asynchronous copy)
+ * into dev_in, the step with the new token's K/V appended (pkv_decode_step_append on the parts of dev_in), and the
+ * copy of dev_out ([B][Hq][d] fp16, device) into host_out (pinned host memory). The caller owns every buffer:
+ * dev_in (device, at least the layout's total, 256-byte aligned), the pools, ws (at least the plan's ws_bytes:
+ * PKV_E_WS_TOO_SMALL otherwise, with nothing enqueued), dev_out and host_out; nothing is allocated. Synchronise the
+ * stream before reading host_out or refilling host_in. If plan_out is not NULL it receives the plan. Errors as
+ * pkv_plan and pkv_decode_step_append; on error nothing is enqueued. The pages describe no such call: it is how a
+ * server feeds the decode step from the host.
+ */
+int pkv_serve_step(const pkv_problem* problem, const pkv_policy* policy, int32_t num_sms, const void* host_in,
+                   void* dev_in, void* k_pool, void* v_pool, float scale, void* ws, size_t ws_bytes, void* dev_out,
+                   void* host_out, void* stream, pkv_plan_t* plan_out);
+
 /* Synchronises `stream`, copies the workspace status word to *status and clears it on the device. */
 int pkv_read_status(void* ws, size_t ws_bytes, void* stream, uint32_t* status);
 

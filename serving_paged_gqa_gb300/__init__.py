@@ -11,4 +11,4 @@ from ._lib import (EXPORTS, LIB_PATH, PKV_MAX_BATCH, PKV_MAX_ROWS_IN_DECODE, PKV
 from .binding import (Plan, Policy, Problem, alloc_workspace, decode, make_problem, pkv_build_worklist,  # noqa: F401
                       pkv_check_problem, pkv_decode, pkv_decode_step, pkv_decode_step_append, pkv_decode_step_static,
                       pkv_merge, pkv_plan, pkv_plan_fixed, pkv_plan_launches, pkv_policy_default, pkv_read_status,
-                      pkv_strerror, pkv_version, pkv_workspace_init)
+                      pkv_serve_step, pkv_step_input_layout, pkv_strerror, pkv_version, pkv_workspace_init, ServeStep)

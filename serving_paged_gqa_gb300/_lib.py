@@ -37,7 +37,8 @@ VARIANT_NAMES = {PKV_VARIANT_SINGLE: "single", PKV_VARIANT_SPLIT: "split", PKV_V
 EXPORTS = (
     "pkv_version", "pkv_strerror", "pkv_check_problem", "pkv_policy_default", "pkv_plan", "pkv_plan_fixed",
     "pkv_workspace_init", "pkv_build_worklist", "pkv_decode", "pkv_merge", "pkv_decode_step", "pkv_read_status",
-    "pkv_plan_launches", "pkv_decode_step_static", "pkv_decode_step_append",
+    "pkv_plan_launches", "pkv_decode_step_static", "pkv_decode_step_append", "pkv_step_input_layout",
+    "pkv_serve_step",
 )
 
 PKV_STATIC_SCRATCH_BYTES = 16 << 20
@@ -104,9 +105,9 @@ def load(path: str | None = None):
         lib.pkv_policy_default.restype = None
         lib.pkv_policy_default.argtypes = [_P(Policy)]
         lib.pkv_plan.restype = ctypes.c_int
-        lib.pkv_plan.argtypes = [_P(Problem), _P(ctypes.c_int32), ctypes.c_int32, _P(Policy), _P(Plan)]
+        lib.pkv_plan.argtypes = [_P(Problem), _vp, ctypes.c_int32, _P(Policy), _P(Plan)]
         lib.pkv_plan_fixed.restype = ctypes.c_int
-        lib.pkv_plan_fixed.argtypes = [_P(Problem), _P(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32,
+        lib.pkv_plan_fixed.argtypes = [_P(Problem), _vp, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.c_int32, ctypes.c_int32, _P(Plan)]
         lib.pkv_workspace_init.restype = ctypes.c_int
         lib.pkv_workspace_init.argtypes = [_vp, ctypes.c_size_t, _vp]
@@ -129,6 +130,11 @@ def load(path: str | None = None):
         lib.pkv_decode_step_static.restype = ctypes.c_int
         lib.pkv_decode_step_static.argtypes = [_P(Plan), _P(Problem), _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp,
                                                _vp, _vp]
+        lib.pkv_step_input_layout.restype = ctypes.c_int
+        lib.pkv_step_input_layout.argtypes = [_P(Problem), _P(ctypes.c_size_t), _P(ctypes.c_size_t)]
+        lib.pkv_serve_step.restype = ctypes.c_int
+        lib.pkv_serve_step.argtypes = [_P(Problem), _P(Policy), ctypes.c_int32, _vp, _vp, _vp, _vp, ctypes.c_float,
+                                       _vp, ctypes.c_size_t, _vp, _vp, _vp, _P(Plan)]
         _lib = lib
         return lib
 

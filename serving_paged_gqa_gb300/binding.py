@@ -19,7 +19,7 @@ __all__ = [
     "Problem", "Plan", "Policy", "pkv_version", "pkv_strerror", "pkv_check_problem", "pkv_policy_default",
     "pkv_plan", "pkv_plan_fixed", "pkv_workspace_init", "pkv_build_worklist", "pkv_decode", "pkv_merge",
     "pkv_decode_step", "pkv_read_status", "pkv_plan_launches", "pkv_decode_step_static", "pkv_decode_step_append",
-    "make_problem",
+    "pkv_step_input_layout", "pkv_serve_step", "ServeStep", "make_problem",
     "alloc_workspace", "decode",
     "PKV_VARIANT_SINGLE", "PKV_VARIANT_SPLIT", "PKV_VARIANT_WORKQUEUE",
 ]
@@ -48,6 +48,8 @@ def _ptr(t: torch.Tensor | None, dtype=None, name: str = "tensor") -> ctypes.c_v
 def _host_lens(seq_lens) -> np.ndarray:
     if isinstance(seq_lens, torch.Tensor):
         seq_lens = seq_lens.detach().cpu().numpy()
+    if isinstance(seq_lens, np.ndarray) and seq_lens.dtype == np.int32 and seq_lens.flags.c_contiguous:
+        return seq_lens
     return np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
 
 
@@ -78,7 +80,7 @@ def pkv_plan(problem: Problem, seq_lens_host, num_sms: int, policy: Policy | Non
     lens = _host_lens(seq_lens_host)
     plan = Plan()
     pol = ctypes.byref(policy) if policy is not None else None
-    check(load().pkv_plan(ctypes.byref(problem), lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), int(num_sms),
+    check(load().pkv_plan(ctypes.byref(problem), lens.ctypes.data, int(num_sms),
                           pol, ctypes.byref(plan)), "pkv_plan")
     return plan
 
@@ -87,7 +89,7 @@ def pkv_plan_fixed(problem: Problem, seq_lens_host, num_sms: int, variant: int, 
                    ctas_per_sm: int = 0) -> Plan:
     lens = _host_lens(seq_lens_host)
     plan = Plan()
-    check(load().pkv_plan_fixed(ctypes.byref(problem), lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+    check(load().pkv_plan_fixed(ctypes.byref(problem), lens.ctypes.data,
                                 int(num_sms), int(variant), int(chunk_pages), int(ctas_per_sm), ctypes.byref(plan)),
           "pkv_plan_fixed")
     return plan
@@ -159,6 +161,62 @@ def pkv_decode_step_static(plan, problem, q, k_pool, v_pool, block_table, seq_le
         _ptr(v_pool, torch.float16, "v_pool"), _ptr(block_table, torch.int32, "block_table"),
         _ptr(seq_lens, torch.int32, "seq_lens"), ctypes.c_float(scale), _ptr(out, torch.float16, "out"),
         _ptr(status, None, "status"), _stream(stream)), "pkv_decode_step_static")
+
+
+def pkv_step_input_layout(problem: Problem) -> tuple[tuple[int, ...], int]:
+    """Byte offsets of (q, k_new, v_new, block_table, seq_lens) in a packed step input, and its total size."""
+    offs = (ctypes.c_size_t * 5)()
+    total = ctypes.c_size_t(0)
+    check(load().pkv_step_input_layout(ctypes.byref(problem), offs, ctypes.byref(total)), "pkv_step_input_layout")
+    return tuple(int(x) for x in offs), int(total.value)
+
+
+def _serve_args(problem, host_in, dev_in, k_pool, v_pool, scale, ws, dev_out, host_out, stream, policy, num_sms,
+                plan_out):
+    if host_in.is_cuda or host_out.is_cuda:
+        raise ValueError("host_in and host_out must be host (pinned) tensors")
+    if not (host_in.is_contiguous() and host_out.is_contiguous()):
+        raise ValueError("host_in and host_out must be contiguous")
+    if host_out.dtype != torch.float16:
+        raise ValueError("host_out must be float16")
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(dev_in.device).multi_processor_count
+    return (ctypes.byref(problem), None if policy is None else ctypes.byref(policy), int(num_sms),
+            ctypes.c_void_p(host_in.data_ptr()), _ptr(dev_in, torch.uint8, "dev_in"),
+            _ptr(k_pool, torch.float16, "k_pool"), _ptr(v_pool, torch.float16, "v_pool"), ctypes.c_float(scale),
+            _ptr(ws, torch.uint8, "ws"), ws.numel(), _ptr(dev_out, torch.float16, "dev_out"),
+            ctypes.c_void_p(host_out.data_ptr()), _stream(stream), ctypes.byref(plan_out))
+
+
+def pkv_serve_step(problem, host_in, dev_in, k_pool, v_pool, scale, ws, dev_out, host_out, stream=None, policy=None,
+                   num_sms=None) -> Plan:
+    """One serving step from host memory (include/pkv.h, pkv_serve_step): plan from the seq_lens in host_in, copy
+    host_in (uint8, pinned, laid out by pkv_step_input_layout) into dev_in, decode with the new token's K/V appended,
+    copy out into host_out (float16 [B, Hq, d], pinned). Asynchronous: synchronise the stream before reading host_out.
+    Returns the plan the step ran."""
+    plan = Plan()
+    check(load().pkv_serve_step(*_serve_args(problem, host_in, dev_in, k_pool, v_pool, scale, ws, dev_out, host_out,
+                                             stream, policy, num_sms, plan)), "pkv_serve_step")
+    return plan
+
+
+class ServeStep:
+    """pkv_serve_step with its arguments marshalled once (a server's per-layer buffers do not change between steps):
+    run() enqueues one step and returns the plan it ran; refill host_in between steps after synchronising."""
+
+    def __init__(self, problem, host_in, dev_in, k_pool, v_pool, scale, ws, dev_out, host_out, stream=None,
+                 policy=None, num_sms=None):
+        self.plan = Plan()
+        self._keep = (problem, host_in, dev_in, k_pool, v_pool, ws, dev_out, host_out, policy)
+        self._args = _serve_args(problem, host_in, dev_in, k_pool, v_pool, scale, ws, dev_out, host_out, stream,
+                                 policy, num_sms, self.plan)
+        self._fn = load().pkv_serve_step
+
+    def run(self) -> Plan:
+        rc = self._fn(*self._args)
+        if rc != 0:
+            check(rc, "pkv_serve_step")
+        return self.plan
 
 
 def pkv_read_status(ws: torch.Tensor, stream=None) -> int:

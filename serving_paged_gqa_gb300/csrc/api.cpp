@@ -284,6 +284,55 @@ extern "C" int pkv_decode_step_append(const pkv_plan_t* plan, const pkv_problem*
                        stream, false);
 }
 
+extern "C" int pkv_step_input_layout(const pkv_problem* pr, size_t offsets[5], size_t* total) {
+    if (!pr || !offsets || !total) return PKV_E_NULLPTR;
+    int rc = pkv_check_problem(pr);
+    if (rc != PKV_OK) return rc;
+    const size_t B = (size_t)pr->batch;
+    const size_t sizes[5] = {B * pr->num_q_heads * pr->head_dim * 2, B * pr->num_kv_heads * pr->head_dim * 2,
+                             B * pr->num_kv_heads * pr->head_dim * 2, B * (size_t)pr->max_pages_per_seq * 4, B * 4};
+    size_t off = 0;
+    for (int i = 0; i < 5; ++i) {
+        offsets[i] = off;
+        off += (sizes[i] + kWsAlign - 1) / kWsAlign * kWsAlign;
+    }
+    *total = off;
+    return PKV_OK;
+}
+
+extern "C" int pkv_serve_step(const pkv_problem* pr, const pkv_policy* policy, int32_t num_sms, const void* host_in,
+                              void* dev_in, void* k_pool, void* v_pool, float scale, void* ws, size_t ws_bytes,
+                              void* dev_out, void* host_out, void* stream, pkv_plan_t* plan_out) {
+    if (!pr || !host_in || !dev_in || !ws || !dev_out || !host_out) return PKV_E_NULLPTR;
+    size_t off[5], total = 0;
+    int rc = pkv_step_input_layout(pr, off, &total);
+    if (rc != PKV_OK) return rc;
+    if (!aligned(dev_in, kWsAlign)) return PKV_E_ALIGN;
+    if (!aligned(host_in, 4)) return PKV_E_ALIGN;
+    // the plan, from the lengths in the host copy of the input
+    const int32_t* lens_host = reinterpret_cast<const int32_t*>(static_cast<const char*>(host_in) + off[4]);
+    pkv_plan_t plan;
+    rc = pkv_plan(pr, lens_host, num_sms, policy, &plan);
+    if (rc != PKV_OK) return rc;
+    if ((int64_t)ws_bytes < plan.ws_bytes) return PKV_E_WS_TOO_SMALL;
+    if (plan_out) *plan_out = plan;
+    char* d = static_cast<char*>(dev_in);
+    rc = check_decode_args(&plan, pr, d + off[0], k_pool, v_pool, reinterpret_cast<const int32_t*>(d + off[3]),
+                           reinterpret_cast<const int32_t*>(d + off[4]), scale, ws, ws_bytes, dev_out);
+    if (rc != PKV_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pr->batch > 0 && cudaMemcpyAsync(dev_in, host_in, total, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return PKV_E_CUDA;
+    rc = decode_step(&plan, pr, d + off[0], d + off[1], d + off[2], k_pool, v_pool,
+                     reinterpret_cast<const int32_t*>(d + off[3]), reinterpret_cast<const int32_t*>(d + off[4]), scale,
+                     ws, ws_bytes, dev_out, stream, false);
+    if (rc != PKV_OK) return rc;
+    const size_t out_bytes = (size_t)pr->batch * pr->num_q_heads * pr->head_dim * 2;
+    if (out_bytes > 0 && cudaMemcpyAsync(host_out, dev_out, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return PKV_E_CUDA;
+    return PKV_OK;
+}
+
 extern "C" int pkv_read_status(void* ws, size_t ws_bytes, void* stream, uint32_t* status) {
     if (!ws || !status) return PKV_E_NULLPTR;
     if (ws_bytes < sizeof(pkv_ws_header)) return PKV_E_WS_TOO_SMALL;

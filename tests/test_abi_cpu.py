@@ -179,3 +179,28 @@ def test_calibration_model_mirrors_the_planner():
                 best = got if best is None else min(best, got)
         chosen = pkv.pkv_plan(pr, lens, 152)
         assert chosen.predicted_us <= best * (1 + 1e-12)
+
+
+def test_step_input_layout_parts_are_aligned_and_disjoint():
+    """The packed serving input: q, k_new, v_new, block table, lengths, each on a 256-byte boundary, in that order,
+    each part as large as its tensor."""
+    B, Hq, Hkv, d, maxp = 5, 32, 8, 128, 37
+    pr = pkv.make_problem(B, Hq, Hkv, d, 16, 1000, maxp)
+    offs, total = pkv.pkv_step_input_layout(pr)
+    sizes = [B * Hq * d * 2, B * Hkv * d * 2, B * Hkv * d * 2, B * maxp * 4, B * 4]
+    assert offs[0] == 0 and all(o % 256 == 0 for o in offs) and total % 256 == 0
+    for i in range(4):
+        assert offs[i] + sizes[i] <= offs[i + 1] < offs[i] + sizes[i] + 256
+    assert offs[4] + sizes[4] <= total < offs[4] + sizes[4] + 256
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_step_input_layout(pkv.make_problem(5, 32, 8, 64, 16, 1000, maxp))  # d = 64 unsupported
+
+
+def test_serve_step_rejects_missing_buffers_before_any_work():
+    """pkv_serve_step returns an error code for null buffers without touching the device."""
+    lib = pkv.load()
+    pr = pkv.make_problem(1, 32, 8, 128, 16, 64, 32)
+    plan = pkv.Plan()
+    rc = lib.pkv_serve_step(ctypes.byref(pr), None, 152, None, None, None, None, ctypes.c_float(0.1), None, 0, None,
+                            None, None, ctypes.byref(plan))
+    assert rc == -3  # PKV_E_NULLPTR

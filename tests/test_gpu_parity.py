@@ -438,3 +438,58 @@ def test_exact_length_bucket_schedule_matches_oracle():
     torch.cuda.synchronize()
     assert pkv.pkv_read_status(ws) == 0
     assert_close(out, ref[order], "exact-length buckets")
+
+
+# ------------------------------------------------------------------------------------------- serving step
+@pytest.mark.parametrize("name,seed,t", [("b8_bimodal", 6, 9), ("b1_bucketed", 5, 3), ("tiny", 1, 0)])
+def test_serve_step_from_host_memory_matches_oracle(name, seed, t):
+    """pkv_serve_step: the packed host input (q, new K/V, block table, lengths) goes to the device, the step runs
+    with the append fused, and out comes back into pinned host memory; it matches the oracle, the new token's slots
+    hold its K/V, the plan is pkv_plan's, a workspace smaller than the plan is refused before anything runs, and a
+    ServeStep run twice matches the oracle each time (bit-identical for static plans; a workqueue's dynamic claims
+    change which consumer warp combines which page, hence the rounding)."""
+    tr = make_trace(name, seed, steps=t + 1)
+    step = Step(tr, t, poison=False)
+    ref = step.reference()
+    B, Hq, Hkv, d = tr.batch, tr.hq, tr.hkv, tr.d
+    rows = torch.arange(B)
+    L = torch.from_numpy(step.lens_host.astype(np.int64))
+    phys = step.bt.cpu()[rows, (L - 1) // 16].cuda().long()
+    slot = ((L - 1) % 16).cuda()
+    k_new = step.k[phys, slot].clone()
+    v_new = step.v[phys, slot].clone()
+    step.k[phys, slot] = float("nan")
+    step.v[phys, slot] = float("nan")
+    offs, total = pkv.pkv_step_input_layout(step.problem)
+    host_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    for i, part in enumerate((step.q.cpu(), k_new.cpu(), v_new.cpu(), torch.from_numpy(step.bt_host),
+                              torch.from_numpy(step.lens_host))):
+        raw = part.contiguous().view(torch.uint8).reshape(-1)
+        host_in[offs[i]:offs[i] + raw.numel()] = raw
+    dev_in = torch.empty(total, dtype=torch.uint8, device="cuda")
+    dev_out = torch.empty((B, Hq, d), dtype=torch.float16, device="cuda")
+    host_out = torch.full((B, Hq, d), float("nan"), dtype=torch.float16).pin_memory()
+    want = step.plan()
+    small = pkv.alloc_workspace(256)
+    with pytest.raises(pkv.PkvError) as err:
+        pkv.pkv_serve_step(step.problem, host_in, dev_in, step.k, step.v, step.scale, small, dev_out, host_out)
+    assert err.value.code == -4 and torch.isnan(host_out.float()).all()  # PKV_E_WS_TOO_SMALL, nothing ran
+    ws = pkv.alloc_workspace(want.ws_bytes)
+    plan = pkv.pkv_serve_step(step.problem, host_in, dev_in, step.k, step.v, step.scale, ws, dev_out, host_out)
+    torch.cuda.synchronize()
+    assert pkv.pkv_read_status(ws) == 0
+    assert (plan.variant, plan.chunk_pages, plan.num_tasks, plan.fuse_merge) == \
+        (want.variant, want.chunk_pages, want.num_tasks, want.fuse_merge)
+    assert_close(host_out.cuda(), ref, f"{name} serve step")
+    assert torch.equal(step.k[phys, slot].view(torch.int16), k_new.view(torch.int16))
+    assert torch.equal(step.v[phys, slot].view(torch.int16), v_new.view(torch.int16))
+    first = host_out.clone()
+    runner = pkv.ServeStep(step.problem, host_in, dev_in, step.k, step.v, step.scale, ws, dev_out, host_out)
+    for i in range(2):
+        host_out.fill_(float("nan"))
+        runner.run()
+        torch.cuda.synchronize()
+        assert_close(host_out.cuda(), ref, f"{name} ServeStep run {i}")
+        if plan.variant != WQ:
+            assert torch.equal(host_out.view(torch.int16), first.view(torch.int16))
+    assert pkv.pkv_read_status(ws) == 0
