@@ -274,14 +274,16 @@ int pkv_step_input_layout(const pkv_problem* problem, size_t offsets[5], size_t*
 /*
  * One serving step of a layer from host memory in a single call: plans the step (pkv_plan with `policy`, NULL = the
  * built-in constants, on the seq_lens of host_in, which the CPU reads during the call), then enqueues on `stream` the
- * copy of the packed input host_in (layout of pkv_step_input_layout; pinned host memory for an asynchronous copy)
- * into dev_in, the step with the new token's K/V appended (pkv_decode_step_append on the parts of dev_in), and the
- * copy of dev_out ([B][Hq][d] fp16, device) into host_out (pinned host memory). The caller owns every buffer:
- * dev_in (device, at least the layout's total, 256-byte aligned), the pools, ws (at least the plan's ws_bytes:
- * PKV_E_WS_TOO_SMALL otherwise, with nothing enqueued), dev_out and host_out; nothing is allocated. Synchronise the
- * stream before reading host_out or refilling host_in. If plan_out is not NULL it receives the plan. Errors as
- * pkv_plan and pkv_decode_step_append; on error nothing is enqueued. The pages describe no such call: it is how a
- * server feeds the decode step from the host.
+ * transfer of the packed input host_in (layout of pkv_step_input_layout) into dev_in, the step with the new token's
+ * K/V appended (pkv_decode_step_append on the parts of dev_in), and the transfer of out ([B][Hq][d] fp16) into
+ * host_out. Page-locked host buffers mapped into the device's address space (cudaHostAlloc, torch's pin_memory) are
+ * moved by the GPU itself: a copy kernel reads host_in through its device address, and the step stores out straight
+ * into host_out (dev_out is then not written); other host buffers go through cudaMemcpyAsync (dev_out receives out
+ * first). The caller owns every buffer: host_in and host_out (16-byte aligned), dev_in (device, at least the
+ * layout's total, 256-byte aligned), the pools, ws (at least the plan's ws_bytes: PKV_E_WS_TOO_SMALL otherwise, with
+ * nothing enqueued) and dev_out; nothing is allocated. Synchronise the stream before reading host_out or refilling
+ * host_in. If plan_out is not NULL it receives the plan. Errors as pkv_plan and pkv_decode_step_append; on error
+ * nothing is enqueued. The pages describe no such call: it is how a server feeds the decode step from the host.
  */
 int pkv_serve_step(const pkv_problem* problem, const pkv_policy* policy, int32_t num_sms, const void* host_in,
                    void* dev_in, void* k_pool, void* v_pool, float scale, void* ws, size_t ws_bytes, void* dev_out,

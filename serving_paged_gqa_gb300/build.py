@@ -16,7 +16,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_DIR = os.path.join(HERE, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libpkv.so")
 
-SOURCES = ["api.cpp", "plan.cpp", "build_worklist.cu", "decode.cu", "merge.cu", "static_scratch.cu"]
+SOURCES = ["api.cpp", "plan.cpp", "build_worklist.cu", "decode.cu", "merge.cu", "static_scratch.cu", "stage.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

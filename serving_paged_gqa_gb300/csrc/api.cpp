@@ -300,6 +300,21 @@ extern "C" int pkv_step_input_layout(const pkv_problem* pr, size_t offsets[5], s
     return PKV_OK;
 }
 
+namespace {
+
+// The device-visible address of page-locked host memory (mapped into the device's address space), or nullptr for
+// any other pointer (pageable host memory, device memory, unknown): such buffers are moved with cudaMemcpyAsync.
+const void* mapped_host_address(const void* p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // an unregistered pointer is not an error of this call
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+}  // namespace
+
 extern "C" int pkv_serve_step(const pkv_problem* pr, const pkv_policy* policy, int32_t num_sms, const void* host_in,
                               void* dev_in, void* k_pool, void* v_pool, float scale, void* ws, size_t ws_bytes,
                               void* dev_out, void* host_out, void* stream, pkv_plan_t* plan_out) {
@@ -307,8 +322,8 @@ extern "C" int pkv_serve_step(const pkv_problem* pr, const pkv_policy* policy, i
     size_t off[5], total = 0;
     int rc = pkv_step_input_layout(pr, off, &total);
     if (rc != PKV_OK) return rc;
-    if (!aligned(dev_in, kWsAlign)) return PKV_E_ALIGN;
-    if (!aligned(host_in, 4)) return PKV_E_ALIGN;
+    if (!aligned(dev_in, kWsAlign) || !aligned(dev_out, 16)) return PKV_E_ALIGN;
+    if (!aligned(host_in, 16) || !aligned(host_out, 16)) return PKV_E_ALIGN;
     // the plan, from the lengths in the host copy of the input
     const int32_t* lens_host = reinterpret_cast<const int32_t*>(static_cast<const char*>(host_in) + off[4]);
     pkv_plan_t plan;
@@ -317,18 +332,27 @@ extern "C" int pkv_serve_step(const pkv_problem* pr, const pkv_policy* policy, i
     if ((int64_t)ws_bytes < plan.ws_bytes) return PKV_E_WS_TOO_SMALL;
     if (plan_out) *plan_out = plan;
     char* d = static_cast<char*>(dev_in);
+    // Page-locked host buffers mapped into the device's address space are read and written by kernels directly
+    // (the input by a copy kernel, out by the step's own output stores); others go through cudaMemcpyAsync.
+    const void* in_mapped = mapped_host_address(host_in);
+    void* out_mapped = const_cast<void*>(mapped_host_address(host_out));
+    void* out = out_mapped ? out_mapped : dev_out;
     rc = check_decode_args(&plan, pr, d + off[0], k_pool, v_pool, reinterpret_cast<const int32_t*>(d + off[3]),
-                           reinterpret_cast<const int32_t*>(d + off[4]), scale, ws, ws_bytes, dev_out);
+                           reinterpret_cast<const int32_t*>(d + off[4]), scale, ws, ws_bytes, out);
     if (rc != PKV_OK) return rc;
+    if (pr->batch == 0) return PKV_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (pr->batch > 0 && cudaMemcpyAsync(dev_in, host_in, total, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    if (in_mapped) {
+        if (launch_stage_copy(in_mapped, dev_in, total, stream) != cudaSuccess) return PKV_E_CUDA;
+    } else if (cudaMemcpyAsync(dev_in, host_in, total, cudaMemcpyHostToDevice, s) != cudaSuccess) {
         return PKV_E_CUDA;
+    }
     rc = decode_step(&plan, pr, d + off[0], d + off[1], d + off[2], k_pool, v_pool,
                      reinterpret_cast<const int32_t*>(d + off[3]), reinterpret_cast<const int32_t*>(d + off[4]), scale,
-                     ws, ws_bytes, dev_out, stream, false);
+                     ws, ws_bytes, out, stream, false);
     if (rc != PKV_OK) return rc;
     const size_t out_bytes = (size_t)pr->batch * pr->num_q_heads * pr->head_dim * 2;
-    if (out_bytes > 0 && cudaMemcpyAsync(host_out, dev_out, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    if (!out_mapped && cudaMemcpyAsync(host_out, dev_out, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return PKV_E_CUDA;
     return PKV_OK;
 }

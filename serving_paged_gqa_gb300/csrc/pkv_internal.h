@@ -69,6 +69,9 @@ struct MergeParams {
 int launch_decode(const DecodeParams& p, int group, int grid, bool pdl, void* stream);
 int launch_build(const BuildParams& p, int grid, void* stream);
 int launch_merge(const MergeParams& p, void* stream);
+// Copies `bytes` (a multiple of 16, both addresses 16-byte aligned) from src to dst on the device; src may be pinned
+// host memory through its device-visible address.
+int launch_stage_copy(const void* src, void* dst, size_t bytes, void* stream);
 
 // Validation shared by pkv_decode and the step entry points (PKV_OK or a PKV_E_* code; enqueues nothing).
 int check_decode_args(const pkv_plan_t* plan, const pkv_problem* pr, const void* q, const void* k_pool,

@@ -170,10 +170,14 @@ def test_edge_lengths_and_empty_rows():
 def test_group_sizes(hq, hkv):
     step = Step(_Lens([40, 300, 17], hkv=hkv, hq=hq, seed=hq * 10 + hkv).trace, 0)
     ref = step.reference()
-    for variant, chunk in ((SINGLE, 1), (SPLIT, 4), (WQ, 2)):
-        out, _, status = step.run(step.plan(variant, chunk))
-        assert status == 0
-        assert_close(out, ref, f"G={hq // hkv} variant {variant}")
+    for variant, chunk in ((SINGLE, 1), (SPLIT, 4), (WQ, 2), (SPLIT, 1)):
+        for fused in ((0,) if variant == SINGLE else (0, 1)):  # both merges: the merge task folds G heads per state
+            plan = step.plan(variant, chunk)
+            if variant != SINGLE:
+                plan.fuse_merge = fused
+            out, _, status = step.run(plan)
+            assert status == 0
+            assert_close(out, ref, f"G={hq // hkv} variant {variant} c={chunk} fused={fused}")
 
 
 def test_partial_states_match_oracle_split_states():
