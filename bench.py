@@ -511,10 +511,11 @@ def run_e2e(pkv, torch, wl, idx, args, sms, flush, stream, dev):
 
 
 def run_multilayer(pkv, torch, args, sms, dev, stream, peak, name="b8_bimodal", seed=5, layers=8):
-    """Decode loop of an 8-layer model's attention: per step and layer, the new token's K/V appended into that layer's
-    pools and the layer's attention, all inside pkv_decode_step_append. The layers share the trace's block table and
-    lengths; each has its own pools (sized to the trace, pages drawn by the trace's permutation) and the same
-    contents, so every layer reads its own K/V from HBM (the layers' K/V together exceed the L2)."""
+    """Decode loop of a `layers`-layer model's attention: per step and layer, the new token's K/V appended into that
+    layer's pools and the layer's attention, all inside pkv_decode_step_append, the layers' steps back to back on the
+    stream with one event pair around the whole step. The layers share the trace's block table and lengths; each has
+    its own pools (sized to the trace, pages drawn by the trace's permutation) and the same contents, so every layer
+    reads its own K/V from HBM (the layers' K/V together exceed the L2)."""
     import math as _m
 
     from workloads import make_trace
@@ -763,6 +764,10 @@ def run_ours(args):
     if names:
         torch.cuda.empty_cache()
         subs["multilayer_b8_bimodal_8layers"] = run_multilayer(pkv, torch, args, sms, dev, stream, peak)
+        for seed in (5, 7):  # B1 starting at 4096 and at 32768 tokens; 16 layers so that their K/V exceed the L2
+            torch.cuda.empty_cache()
+            subs[f"multilayer_b1_bucketed_seed{seed}_16layers"] = run_multilayer(
+                pkv, torch, args, sms, dev, stream, peak, name="b1_bucketed", seed=seed, layers=16)
         torch.cuda.empty_cache()
         subs["schedules_b8_bimodal"] = run_schedules(pkv, torch, args, sms, dev, flush, stream)
     line["traces"] = subs
