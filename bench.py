@@ -559,26 +559,37 @@ def run_multilayer(pkv, torch, args, sms, dev, stream, peak, name="b8_bimodal", 
                        vp(vn.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()), vp(bt.data_ptr()), vp(ln.data_ptr()),
                        ctypes.c_float(scale), vp(ws.data_ptr()), ws.numel(), vp(out.data_ptr()),
                        vp(stream.cuda_stream)) for k, v in pools])
-    for layer_calls in calls[:2]:
-        for a in layer_calls:
-            _call(lib.pkv_decode_step_append, a, "pkv_decode_step_append")
-    torch.cuda.synchronize()
-    ev = []
     spin = int(args.spin_us * 4 * 1e-6 * 2.0e9)
-    for layer_calls in calls:
-        torch.cuda._sleep(spin)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for a in layer_calls:
-            _call(lib.pkv_decode_step_append, a, "pkv_decode_step_append")
-        e1.record(stream)
-        ev.append((e0, e1))
-    torch.cuda.synchronize()
+
+    def run(overlap):
+        # layers after the first may start while the previous layer's last kernel finishes (PKV_PLAN_OVERLAP_PREV):
+        # their pools, block table and lengths are not written by it
+        for st in steps:
+            st[0].flags = pkv.PKV_PLAN_OVERLAP_PREV if overlap else 0
+        for layer_calls in calls[:2]:
+            for a in layer_calls:
+                _call(lib.pkv_decode_step_append, a, "pkv_decode_step_append")
+        torch.cuda.synchronize()
+        ev = []
+        for layer_calls in calls:
+            torch.cuda._sleep(spin)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for a in layer_calls:
+                _call(lib.pkv_decode_step_append, a, "pkv_decode_step_append")
+            e1.record(stream)
+            ev.append((e0, e1))
+        torch.cuda.synchronize()
+        return np.array([a.elapsed_time(b) * 1e3 for a, b in ev])
+
+    step_us_plain = run(False)
+    step_us = run(True)
     status = pkv.pkv_read_status(ws)
-    step_us = np.array([a.elapsed_time(b) * 1e3 for a, b in ev])
     kv = np.array([st[6] for st in steps]) * layers
     return {"layers": layers, "trace": name, "seed": seed, "steps": K, "tokens_per_s": B * K / (step_us.sum() * 1e-6),
             "step_us_mean": float(step_us.mean()), "layer_us_mean": float(step_us.mean()) / layers,
+            "layer_us_mean_without_overlap": float(step_us_plain.mean()) / layers,
+            "overlap": "layers after the first launched with PKV_PLAN_OVERLAP_PREV",
             "step_frac": float(kv.sum() / (step_us.sum() * 1e-6)) / 1e9 / peak,
             "launches_per_step": layers * pkv.pkv_plan_launches(steps[0][0]),
             "variants_used": sorted({pkv.VARIANT_NAMES[st[0].variant] for st in steps}),

@@ -131,14 +131,15 @@ typedef struct pkv_plan_t {
     int32_t fuse_merge;  /* split / workqueue: 1 = pkv_decode merges the split states itself (the CTA whose task of
                             a (row, KV head) finishes last runs the pair's merge as one more task: its states go
                             through that CTA's page ring, and it writes out; pkv_merge is then a no-op);
-                            0 = pkv_decode writes partial states only and pkv_merge combines them. The planners set
-                            1; a caller may set 0 (the workspace layout does not depend on it). */
+                            0 = pkv_decode writes partial states only and pkv_merge combines them. The planners pick
+                            the mode their cost model predicts faster; a caller may change it (the workspace layout
+                            does not depend on it). */
     int32_t list_in_decode; /* workqueue: 1 = the decode kernel derives the compact list itself from seq_lens (every
                                CTA scans the per-row split counts into shared memory; CTA 0 publishes row_off /
                                row_splits / task_count), so no pkv_build_worklist launch is needed; 0 = the decode
                                runs the list pkv_build_worklist wrote. The planners set 1 when B <= PKV_MAX_ROWS_IN_DECODE.
                                Both give the same task order (b, h_kv, s). */
-    int32_t reserved;
+    int32_t flags;          /* PKV_PLAN_* bits, 0 from the planners */
     pkv_problem problem; /* copy of the problem the plan was made for; later calls must pass an equal one */
     int64_t task_capacity;  /* task slots reserved in the workspace */
     int64_t state_capacity; /* partial-state slots reserved in the workspace */
@@ -170,6 +171,17 @@ typedef struct pkv_ws_header {
     uint32_t ctas_done;   /* decode CTAs that finished claiming (workqueue); back to 0 after every decode */
     uint32_t reserved[60];
 } pkv_ws_header;
+
+/*
+ * Plan flag: the step may start while the kernel enqueued just before it on the same stream is still running
+ * (programmatic dependent launch), so its CTAs start, read their block-table entries and lengths and begin copying
+ * K/V pages while that kernel finishes; q, k_new and v_new are read, and out and the workspace written, only after
+ * that kernel has completed (griddepcontrol.wait). Set it only if that kernel writes none of block_table, seq_lens,
+ * k_pool and v_pool (typical of a layer loop: the previous layer produced q, the block table and lengths were
+ * written before the first layer). Ignored by plans that run the worklist builder (workqueue with list_in_decode
+ * = 0). The separate merge kernel lets the next launch start early as well.
+ */
+#define PKV_PLAN_OVERLAP_PREV 0x1u
 
 /* Library version (PKV_VERSION). */
 int pkv_version(void);

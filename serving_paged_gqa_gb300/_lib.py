@@ -28,6 +28,8 @@ PKV_STATUS_TASKS = 0x8
 PKV_MAX_BATCH = 4096
 PKV_MAX_ROWS_IN_DECODE = 256
 
+PKV_PLAN_OVERLAP_PREV = 0x1
+
 PKV_VARIANT_SINGLE = 0
 PKV_VARIANT_SPLIT = 1
 PKV_VARIANT_WORKQUEUE = 2
@@ -66,7 +68,7 @@ class Plan(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int32), ("chunk_pages", ctypes.c_int32), ("num_splits", ctypes.c_int32),
                 ("num_tasks", ctypes.c_int32), ("grid_ctas", ctypes.c_int32), ("group", ctypes.c_int32),
                 ("num_sms", ctypes.c_int32), ("fuse_merge", ctypes.c_int32), ("list_in_decode", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("problem", Problem),
+                ("flags", ctypes.c_int32), ("problem", Problem),
                 ("task_capacity", ctypes.c_int64), ("state_capacity", ctypes.c_int64),
                 ("ws_bytes", ctypes.c_int64), ("off_counters", ctypes.c_int64), ("off_row_off", ctypes.c_int64),
                 ("off_row_splits", ctypes.c_int64),

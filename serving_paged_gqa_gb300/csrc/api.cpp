@@ -27,6 +27,7 @@ int check_plan(const pkv_plan_t* plan, const pkv_problem* pr, const void* ws, si
         (plan->list_in_decode != 0 && plan->list_in_decode != 1))
         return PKV_E_INVAL;
     if (plan->list_in_decode && pr->batch > PKV_MAX_ROWS_IN_DECODE) return PKV_E_UNSUPPORTED;
+    if ((uint32_t)plan->flags & ~PKV_PLAN_OVERLAP_PREV) return PKV_E_INVAL;
     if (plan->off_counters < (int64_t)sizeof(pkv_ws_header) ||
         plan->off_counters + 4 * (int64_t)pr->batch * pr->num_kv_heads > plan->ws_bytes)
         return PKV_E_INVAL;
@@ -240,8 +241,11 @@ int pkv::decode_launch(const pkv_plan_t* plan, const pkv_problem* pr, const void
     p.list_in_decode = plan->variant == PKV_VARIANT_WORKQUEUE && plan->list_in_decode;
     p.scale_log2 = scale * 1.4426950408889634f;
     // The workqueue decode follows its builder: let it start while the builder runs (it reads the builder's output
-    // only after griddepcontrol.wait).
-    const bool pdl = plan->variant == PKV_VARIANT_WORKQUEUE && !plan->list_in_decode;
+    // only after griddepcontrol.wait). Otherwise it may start early only if the plan says the kernel before it writes
+    // none of what the decode reads before that wait.
+    const bool builder = plan->variant == PKV_VARIANT_WORKQUEUE && !plan->list_in_decode;
+    const bool pdl = builder || ((uint32_t)plan->flags & PKV_PLAN_OVERLAP_PREV);
+    p.overlap_prev = !builder && ((uint32_t)plan->flags & PKV_PLAN_OVERLAP_PREV) ? 1 : 0;
     return cuda_rc(launch_decode(p, plan->group, plan->grid_ctas, pdl, stream));
 }
 

@@ -404,7 +404,7 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
         if (warp == NCW + 2 && lane == 0) {
             for (int i = 0; i < NTS; ++i) mbar_init(&tq[i], 1);
             mbar_fence_init();
-            if (pre_ok) {
+            if (pre_ok && !p.overlap_prev) {  // overlapping the kernel before: q may still be in the making
                 mbar_arrive_expect_tx(&tq[0], G * kRowBytes);
                 bulk_g2s(smem + L::off_q,
                          static_cast<const __half*>(p.q) + ((size_t)k.b * p.Hq + (size_t)k.h * G) * kHeadDim,
@@ -618,6 +618,7 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
             // the row length and the task's first block-table entries, fetched together (for the CTA's first static
             // task they were read before the CTA barrier)
             const bool prefetched = first && pre_ok && !bad;
+            const bool q_copied = prefetched && !p.overlap_prev;  // the first task's query rows are in slot 0
             const int nent = max(0, min(min(pe, p.max_pages) - pb, kSlotEntries));
             const int ent = prefetched ? pre_ent : (lane < nent ? p.block_table[(size_t)b * p.max_pages + pb + lane] : -1);
             int len = prefetched ? pre_len : p.seq_lens[b];
@@ -659,7 +660,7 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
             // The CTA's first static task had its rows copied before the CTA barrier.
             if (lane == 0) {
                 mbar_arrive(&tmeta[ts]);
-                if (!prefetched) {
+                if (!q_copied) {
                     if (!bad) {
                         mbar_arrive_expect_tx(&tq[ts], G * kRowBytes);
                         bulk_g2s(smem + L::off_q + ts * L::kQRowsBytes,
@@ -675,7 +676,7 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
         }
         // Before the warp leaves, every query copy it issued has landed (only after an abort can one be pending),
         // including the first task's copy when the warp stopped before publishing its slot.
-        if (tseq == 0 && pre_ok) warp_drain(&tq[0], 0);
+        if (tseq == 0 && pre_ok && !p.overlap_prev) warp_drain(&tq[0], 0);
         for (int j = max(0, tseq - NTS); j < tseq; ++j) warp_drain(&tq[j % NTS], (j / NTS) & 1);
         // Workqueue with the merge fused: rows without tokens have no task, so their (zero) output is written here.
         if (wq && p.fuse_merge) {

@@ -29,6 +29,9 @@ __global__ void __launch_bounds__(kWarps * 32) merge_kernel(const MergeParams p)
     __shared__ float s_max[kWarps];
     __shared__ float4 s_acc[kWarps][32];
     __shared__ float s_den[kWarps];
+    // a grid launched after this one to overlap it (a decode of the next layer) may start now: it reads what this
+    // grid writes only after waiting for it
+    grid_launch_dependents();
     grid_dependency_wait();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int pair = blockIdx.x;

@@ -497,3 +497,31 @@ def test_serve_step_from_host_memory_matches_oracle(name, seed, t):
         if plan.variant != WQ:
             assert torch.equal(host_out.view(torch.int16), first.view(torch.int16))
     assert pkv.pkv_read_status(ws) == 0
+
+
+@pytest.mark.parametrize("name,seed,t,variant,chunk,fused", [
+    ("b1_bucketed", 5, 4, SPLIT, 8, 0), ("b8_bimodal", 6, 2, WQ, 16, 0), ("b8_zipf", 7, 9, WQ, 12, 1),
+    ("tiny", 2, 0, SINGLE, 1, 0), ("b4_bimodal", 5, 3, SPLIT, 64, 1)])
+def test_overlapping_layers_read_the_previous_layers_output(name, seed, t, variant, chunk, fused):
+    """A layer loop with PKV_PLAN_OVERLAP_PREV: layer l + 1's query rows are layer l's output buffer (poisoned with
+    NaN before the loop), so a step that read q before the previous layer's last kernel had finished would produce
+    NaN or the wrong rows. Every layer matches the oracle run on the query rows the previous layer produced."""
+    tr = make_trace(name, seed, steps=t + 1)
+    step = Step(tr, t)
+    plan = step.plan(variant, chunk)
+    if variant != SINGLE:
+        plan.fuse_merge = fused
+    ws = pkv.alloc_workspace(plan.ws_bytes)
+    layers = 4
+    bufs = [step.q.clone()] + [torch.full_like(step.q, float("nan")) for _ in range(layers)]
+    kp, vp = tr.host_pools()
+    for layer in range(layers):
+        plan.flags = pkv.PKV_PLAN_OVERLAP_PREV if layer else 0
+        pkv.pkv_decode_step(plan, step.problem, bufs[layer], step.k, step.v, step.bt, step.lens, step.scale, ws,
+                            bufs[layer + 1])
+    torch.cuda.synchronize()
+    assert pkv.pkv_read_status(ws) == 0
+    for layer in range(layers):
+        q_in = bufs[layer].cpu().numpy()
+        ref = oracle.attention(q_in, kp, vp, step.bt_host, step.lens_host, step.scale)
+        assert_close(bufs[layer + 1], ref, f"{name} layer {layer} variant {variant} fused {fused}")
