@@ -487,6 +487,16 @@ def test_serve_step_from_host_memory_matches_oracle(name, seed, t):
     assert_close(host_out.cuda(), ref, f"{name} serve step")
     assert torch.equal(step.k[phys, slot].view(torch.int16), k_new.view(torch.int16))
     assert torch.equal(step.v[phys, slot].view(torch.int16), v_new.view(torch.int16))
+    # ordinary (pageable) host buffers: the input and out go through cudaMemcpyAsync instead of the GPU's own loads
+    # and stores
+    pageable_out = torch.full((B, Hq, d), float("nan"), dtype=torch.float16)
+    assert not pageable_out.is_pinned()
+    pageable_in = torch.empty(host_in.shape, dtype=torch.uint8)
+    pageable_in.copy_(host_in)
+    assert not pageable_in.is_pinned()
+    pkv.pkv_serve_step(step.problem, pageable_in, dev_in, step.k, step.v, step.scale, ws, dev_out, pageable_out)
+    torch.cuda.synchronize()
+    assert_close(pageable_out.cuda(), ref, f"{name} serve step, pageable host buffers")
     first = host_out.clone()
     runner = pkv.ServeStep(step.problem, host_in, dev_in, step.k, step.v, step.scale, ws, dev_out, host_out)
     for i in range(2):
