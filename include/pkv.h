@@ -138,7 +138,9 @@ typedef struct pkv_plan_t {
                                CTA scans the per-row split counts into shared memory; CTA 0 publishes row_off /
                                row_splits / task_count), so no pkv_build_worklist launch is needed; 0 = the decode
                                runs the list pkv_build_worklist wrote. The planners set 1 when B <= PKV_MAX_ROWS_IN_DECODE.
-                               Both give the same task order (b, h_kv, s). */
+                               Both give the same list and state layout, in (b, h_kv, s) order. The builder's list
+                               is claimed in that order; a list derived in the decode is claimed split by split
+                               within a row (the Hkv tasks of one split, which read the same pages, together). */
     int32_t flags;          /* PKV_PLAN_* bits, 0 from the planners */
     pkv_problem problem; /* copy of the problem the plan was made for; later calls must pass an equal one */
     int64_t task_capacity;  /* task slots reserved in the workspace */
