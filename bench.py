@@ -470,8 +470,10 @@ def run_e2e(pkv, torch, wl, idx, args, sms, flush, stream, dev):
     inputs (q, the new token's K/V, block table, lengths) sit packed in pinned host memory (pkv_step_input_layout);
     one pkv_serve_step call plans the step from the host lengths, copies the packed input to the device, runs the
     decode with the new token's K/V appended into its page slot, and copies out back to pinned host memory; then the
-    stream is synchronised. The call's arguments are marshalled once per step buffer (ServeStep), as a server keeps
-    its per-layer buffers."""
+    stream is synchronised. The buffers are bound once per step buffer, as a server keeps its per-layer buffers:
+    through a ServeSession (the step's launches replayed from the CUDA graph of its plan, captured in an untimed
+    first run: a decode loop's plan repeats for chunk_pages * page_size steps) for the reported value, and through
+    ServeStep (plan and launches enqueued by the call every step) for comparison."""
     B, Hq, Hkv, d, ps = wl.B, wl.Hq, wl.Hkv, wl.d, wl.ps
     scale = 1.0 / math.sqrt(d)
     out_d = torch.empty((B, Hq, d), dtype=torch.float16, device=dev)
@@ -502,23 +504,39 @@ def run_e2e(pkv, torch, wl, idx, args, sms, flush, stream, dev):
             raw = np.ascontiguousarray(part).view(np.uint8).ravel()
             buf[o:o + raw.size] = raw
         host_in = torch.from_numpy(buf).pin_memory()
-        runners.append((pkv.ServeStep(problem, host_in, dev_in, kpool, vpool, scale, ws, out_d, out_h, stream,
+        runners.append((pkv.ServeSession(problem, host_in, dev_in, kpool, vpool, scale, ws, out_d, out_h, policy, sms),
+                        pkv.ServeStep(problem, host_in, dev_in, kpool, vpool, scale, ws, out_d, out_h, stream,
                                       policy, sms), total))
-    times = []
-    h2d = d2h = 0
-    for runner, total in runners:
-        flush()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        runner.run()
-        stream.synchronize()
-        times.append(time.perf_counter() - t0)
-        h2d = total
-        d2h = out_h.numel() * 2
+    for session, _, _ in runners:  # graph capture, untimed
+        session.run(stream)
+    stream.synchronize()
+
+    def timed(which):
+        times = []
+        for r in runners:
+            flush()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            r[0].run(stream) if which == 0 else r[1].run()
+            stream.synchronize()
+            times.append(time.perf_counter() - t0)
+        return np.array(times)
+
+    times = timed(0)
+    direct = timed(1)
+    graphs = [r[0].stats() for r in runners]
+    for r in runners:
+        r[0].close()
+    h2d, d2h = runners[-1][2], out_h.numel() * 2
     return {"value": B * len(times) / float(np.sum(times)), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": len(times), "us_per_step": 1e6 * float(np.mean(times)),
-            "timing": "host wall clock per step, synchronize on both sides; one pkv_serve_step call: pkv_plan on the "
-                      "host lengths, H2D of the packed input, decode with the KV append fused, D2H of out"}
+            "graph_replays_timed": int(sum(n - 1 for _, n in graphs)),
+            "direct_us_per_step": 1e6 * float(np.mean(direct)),
+            "direct_value": B * len(direct) / float(np.sum(direct)),
+            "timing": "host wall clock per step, synchronize on both sides; one pkv_session_step call: pkv_plan on "
+                      "the host lengths, then the plan's CUDA graph: the packed input read from pinned host memory "
+                      "into the device, decode with the KV append fused, out stored into pinned host memory; "
+                      "direct_*: the same step through pkv_serve_step, its launches enqueued by the call"}
 
 
 def run_multilayer(pkv, torch, args, sms, dev, stream, peak, name="b8_bimodal", seed=5, layers=8):

@@ -303,6 +303,43 @@ int pkv_serve_step(const pkv_problem* problem, const pkv_policy* policy, int32_t
                    void* dev_in, void* k_pool, void* v_pool, float scale, void* ws, size_t ws_bytes, void* dev_out,
                    void* host_out, void* stream, pkv_plan_t* plan_out);
 
+/* Distinct plans whose captured launches a serving session keeps (least recently used first out). */
+#define PKV_SESSION_GRAPHS 16
+
+/*
+ * Serving session: the buffers of pkv_serve_step bound once (a server's per-layer buffers do not change between
+ * steps), and the step's launches replayed from CUDA graphs. The pages describe no such object; it is how this
+ * library takes the host-side launch cost off a decode loop, where the plan repeats for many steps (a row's split
+ * count changes once every chunk_pages * page_size tokens).
+ *
+ * pkv_session_create validates and binds problem, policy (copied; NULL = the built-in constants), num_sms (> 0) and
+ * the buffers exactly as pkv_serve_step takes them (same layout, alignment and ownership rules; the caller keeps
+ * every buffer alive until pkv_session_destroy); it resolves whether host_in and host_out are mapped page-locked
+ * memory and, if both are, creates one private non-blocking stream for capturing. *session receives the handle
+ * (NULL on error). Errors: PKV_E_NULLPTR, PKV_E_INVAL (num_sms <= 0), PKV_E_ALIGN, pkv_check_problem errors,
+ * PKV_E_CUDA (stream creation).
+ *
+ * pkv_session_step runs one step with the current contents of host_in: pkv_plan on its seq_lens, then, with both
+ * host buffers mapped, the step's launches (input copy kernel, decode with the append, merge) are looked up by the
+ * plan's launch fields (every field of pkv_plan_t but predicted_us and kv_bytes); a plan seen before replays its
+ * graph with one cudaGraphLaunch on `stream`, a new one is captured on the private stream, instantiated, kept (at
+ * most PKV_SESSION_GRAPHS, the least recently used is destroyed) and launched. Otherwise (a pageable host buffer, or
+ * `stream` being captured by the caller) the launches are enqueued on `stream` as pkv_serve_step does. Results,
+ * asynchrony and errors as pkv_serve_step (synchronise `stream` before reading host_out or refilling host_in);
+ * plan_out (optional) receives the plan. One host thread at a time per session.
+ *
+ * pkv_session_stats: graphs captured and graph launches so far. pkv_session_destroy destroys the graphs and the
+ * private stream and frees the handle (NULL is a no-op); no work of the session may be pending on the GPU.
+ */
+typedef struct pkv_session pkv_session;
+
+int pkv_session_create(const pkv_problem* problem, const pkv_policy* policy, int32_t num_sms, const void* host_in,
+                       void* dev_in, void* k_pool, void* v_pool, float scale, void* ws, size_t ws_bytes,
+                       void* dev_out, void* host_out, pkv_session** session);
+int pkv_session_step(pkv_session* session, void* stream, pkv_plan_t* plan_out);
+int pkv_session_stats(const pkv_session* session, int64_t* graphs_captured, int64_t* graph_launches);
+int pkv_session_destroy(pkv_session* session);
+
 /* Synchronises `stream`, copies the workspace status word to *status and clears it on the device. */
 int pkv_read_status(void* ws, size_t ws_bytes, void* stream, uint32_t* status);
 

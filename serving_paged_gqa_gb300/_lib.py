@@ -40,8 +40,10 @@ EXPORTS = (
     "pkv_version", "pkv_strerror", "pkv_check_problem", "pkv_policy_default", "pkv_plan", "pkv_plan_fixed",
     "pkv_workspace_init", "pkv_build_worklist", "pkv_decode", "pkv_merge", "pkv_decode_step", "pkv_read_status",
     "pkv_plan_launches", "pkv_decode_step_static", "pkv_decode_step_append", "pkv_step_input_layout",
-    "pkv_serve_step",
+    "pkv_serve_step", "pkv_session_create", "pkv_session_step", "pkv_session_stats", "pkv_session_destroy",
 )
+
+PKV_SESSION_GRAPHS = 16
 
 PKV_STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -137,6 +139,15 @@ def load(path: str | None = None):
         lib.pkv_serve_step.restype = ctypes.c_int
         lib.pkv_serve_step.argtypes = [_P(Problem), _P(Policy), ctypes.c_int32, _vp, _vp, _vp, _vp, ctypes.c_float,
                                        _vp, ctypes.c_size_t, _vp, _vp, _vp, _P(Plan)]
+        lib.pkv_session_create.restype = ctypes.c_int
+        lib.pkv_session_create.argtypes = [_P(Problem), _P(Policy), ctypes.c_int32, _vp, _vp, _vp, _vp,
+                                           ctypes.c_float, _vp, ctypes.c_size_t, _vp, _vp, _P(_vp)]
+        lib.pkv_session_step.restype = ctypes.c_int
+        lib.pkv_session_step.argtypes = [_vp, _vp, _P(Plan)]
+        lib.pkv_session_stats.restype = ctypes.c_int
+        lib.pkv_session_stats.argtypes = [_vp, _P(ctypes.c_int64), _P(ctypes.c_int64)]
+        lib.pkv_session_destroy.restype = ctypes.c_int
+        lib.pkv_session_destroy.argtypes = [_vp]
         _lib = lib
         return lib
 

@@ -173,6 +173,11 @@ def pkv_step_input_layout(problem: Problem) -> tuple[tuple[int, ...], int]:
 
 def _serve_args(problem, host_in, dev_in, k_pool, v_pool, scale, ws, dev_out, host_out, stream, policy, num_sms,
                 plan_out):
+    return _bind_args(problem, host_in, dev_in, k_pool, v_pool, scale, ws, dev_out, host_out, policy, num_sms) + (
+        _stream(stream), ctypes.byref(plan_out))
+
+
+def _bind_args(problem, host_in, dev_in, k_pool, v_pool, scale, ws, dev_out, host_out, policy, num_sms):
     if host_in.is_cuda or host_out.is_cuda:
         raise ValueError("host_in and host_out must be host (pinned) tensors")
     if not (host_in.is_contiguous() and host_out.is_contiguous()):
@@ -185,7 +190,7 @@ def _serve_args(problem, host_in, dev_in, k_pool, v_pool, scale, ws, dev_out, ho
             ctypes.c_void_p(host_in.data_ptr()), _ptr(dev_in, torch.uint8, "dev_in"),
             _ptr(k_pool, torch.float16, "k_pool"), _ptr(v_pool, torch.float16, "v_pool"), ctypes.c_float(scale),
             _ptr(ws, torch.uint8, "ws"), ws.numel(), _ptr(dev_out, torch.float16, "dev_out"),
-            ctypes.c_void_p(host_out.data_ptr()), _stream(stream), ctypes.byref(plan_out))
+            ctypes.c_void_p(host_out.data_ptr()))
 
 
 def pkv_serve_step(problem, host_in, dev_in, k_pool, v_pool, scale, ws, dev_out, host_out, stream=None, policy=None,
@@ -217,6 +222,51 @@ class ServeStep:
         if rc != 0:
             check(rc, "pkv_serve_step")
         return self.plan
+
+
+class ServeSession:
+    """A serving session (include/pkv.h, pkv_session_*): the buffers of pkv_serve_step bound once; run() plans the
+    step from the seq_lens in host_in and replays the plan's captured CUDA graph (capturing it the first time the
+    plan is seen) when both host buffers are mapped pinned memory, else enqueues the launches directly. Returns the
+    plan it ran. Synchronise the stream before reading host_out or refilling host_in; close() when done."""
+
+    def __init__(self, problem, host_in, dev_in, k_pool, v_pool, scale, ws, dev_out, host_out, policy=None,
+                 num_sms=None):
+        self.plan = Plan()
+        self._keep = (problem, host_in, dev_in, k_pool, v_pool, ws, dev_out, host_out, policy)
+        a = _bind_args(problem, host_in, dev_in, k_pool, v_pool, scale, ws, dev_out, host_out, policy, num_sms)
+        self._lib = load()
+        h = ctypes.c_void_p()
+        check(self._lib.pkv_session_create(*a, ctypes.byref(h)), "pkv_session_create")
+        self._h = h
+        self._streams = {}
+
+    def run(self, stream=None) -> Plan:
+        key = id(stream)
+        args = self._streams.get(key)
+        if args is None:
+            args = self._streams[key] = (self._h, _stream(stream), ctypes.byref(self.plan))
+        rc = self._lib.pkv_session_step(*args)
+        if rc != 0:
+            check(rc, "pkv_session_step")
+        return self.plan
+
+    def stats(self) -> tuple[int, int]:
+        """(graphs captured, graph launches) so far."""
+        c, n = ctypes.c_int64(0), ctypes.c_int64(0)
+        check(self._lib.pkv_session_stats(self._h, ctypes.byref(c), ctypes.byref(n)), "pkv_session_stats")
+        return int(c.value), int(n.value)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            h, self._h = self._h, None
+            check(self._lib.pkv_session_destroy(h), "pkv_session_destroy")
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def pkv_read_status(ws: torch.Tensor, stream=None) -> int:

@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "pkv_internal.h"
 
@@ -317,48 +318,226 @@ const void* mapped_host_address(const void* p) {
     return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
 }
 
+// The buffers of a serving step (everything but the step's contents), validated once.
+struct ServeBind {
+    pkv_problem pr;
+    size_t off[5];
+    size_t total;
+    const void* host_in;
+    void* dev_in;
+    void* k_pool;
+    void* v_pool;
+    float scale;
+    void* ws;
+    size_t ws_bytes;
+    void* dev_out;
+    void* host_out;
+    const void* in_mapped;  // device-visible addresses of the host buffers, or nullptr (copied by cudaMemcpyAsync)
+    void* out_mapped;
+};
+
+int bind_serve(const pkv_problem* pr, const void* host_in, void* dev_in, void* k_pool, void* v_pool, float scale,
+               void* ws, size_t ws_bytes, void* dev_out, void* host_out, ServeBind* sb) {
+    if (!pr || !host_in || !dev_in || !ws || !dev_out || !host_out) return PKV_E_NULLPTR;
+    int rc = pkv_step_input_layout(pr, sb->off, &sb->total);
+    if (rc != PKV_OK) return rc;
+    if (!aligned(dev_in, kWsAlign) || !aligned(dev_out, 16)) return PKV_E_ALIGN;
+    if (!aligned(host_in, 16) || !aligned(host_out, 16)) return PKV_E_ALIGN;
+    sb->pr = *pr;
+    sb->host_in = host_in;
+    sb->dev_in = dev_in;
+    sb->k_pool = k_pool;
+    sb->v_pool = v_pool;
+    sb->scale = scale;
+    sb->ws = ws;
+    sb->ws_bytes = ws_bytes;
+    sb->dev_out = dev_out;
+    sb->host_out = host_out;
+    // Page-locked host buffers mapped into the device's address space are read and written by kernels directly
+    // (the input by a copy kernel, out by the step's own output stores); others go through cudaMemcpyAsync.
+    sb->in_mapped = mapped_host_address(host_in);
+    sb->out_mapped = const_cast<void*>(mapped_host_address(host_out));
+    return PKV_OK;
+}
+
+const int32_t* host_lens(const ServeBind& sb) {
+    return reinterpret_cast<const int32_t*>(static_cast<const char*>(sb.host_in) + sb.off[4]);
+}
+
+int check_serve(const ServeBind& sb, const pkv_plan_t* plan) {
+    if ((int64_t)sb.ws_bytes < plan->ws_bytes) return PKV_E_WS_TOO_SMALL;
+    const char* d = static_cast<const char*>(sb.dev_in);
+    return check_decode_args(plan, &sb.pr, d + sb.off[0], sb.k_pool, sb.v_pool,
+                             reinterpret_cast<const int32_t*>(d + sb.off[3]),
+                             reinterpret_cast<const int32_t*>(d + sb.off[4]), sb.scale, sb.ws, sb.ws_bytes,
+                             sb.out_mapped ? sb.out_mapped : sb.dev_out);
+}
+
+// Enqueues one serving step of `plan` on `s`: the input copy, the decode with the new token appended, the merge and
+// the output copy (arguments checked by check_serve).
+int serve_enqueue(const ServeBind& sb, const pkv_plan_t* plan, cudaStream_t s) {
+    if (sb.pr.batch == 0) return PKV_OK;
+    char* d = static_cast<char*>(sb.dev_in);
+    void* out = sb.out_mapped ? sb.out_mapped : sb.dev_out;
+    if (sb.in_mapped) {
+        if (launch_stage_copy(sb.in_mapped, sb.dev_in, sb.total, s) != cudaSuccess) return PKV_E_CUDA;
+    } else if (cudaMemcpyAsync(sb.dev_in, sb.host_in, sb.total, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+        return PKV_E_CUDA;
+    }
+    int rc = decode_step(plan, &sb.pr, d + sb.off[0], d + sb.off[1], d + sb.off[2], sb.k_pool, sb.v_pool,
+                         reinterpret_cast<const int32_t*>(d + sb.off[3]),
+                         reinterpret_cast<const int32_t*>(d + sb.off[4]), sb.scale, sb.ws, sb.ws_bytes, out, s, false);
+    if (rc != PKV_OK) return rc;
+    const size_t out_bytes = (size_t)sb.pr.batch * sb.pr.num_q_heads * sb.pr.head_dim * 2;
+    if (!sb.out_mapped && cudaMemcpyAsync(sb.host_out, sb.dev_out, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return PKV_E_CUDA;
+    return PKV_OK;
+}
+
 }  // namespace
 
 extern "C" int pkv_serve_step(const pkv_problem* pr, const pkv_policy* policy, int32_t num_sms, const void* host_in,
                               void* dev_in, void* k_pool, void* v_pool, float scale, void* ws, size_t ws_bytes,
                               void* dev_out, void* host_out, void* stream, pkv_plan_t* plan_out) {
-    if (!pr || !host_in || !dev_in || !ws || !dev_out || !host_out) return PKV_E_NULLPTR;
-    size_t off[5], total = 0;
-    int rc = pkv_step_input_layout(pr, off, &total);
+    ServeBind sb;
+    int rc = bind_serve(pr, host_in, dev_in, k_pool, v_pool, scale, ws, ws_bytes, dev_out, host_out, &sb);
     if (rc != PKV_OK) return rc;
-    if (!aligned(dev_in, kWsAlign) || !aligned(dev_out, 16)) return PKV_E_ALIGN;
-    if (!aligned(host_in, 16) || !aligned(host_out, 16)) return PKV_E_ALIGN;
-    // the plan, from the lengths in the host copy of the input
-    const int32_t* lens_host = reinterpret_cast<const int32_t*>(static_cast<const char*>(host_in) + off[4]);
-    pkv_plan_t plan;
-    rc = pkv_plan(pr, lens_host, num_sms, policy, &plan);
+    pkv_plan_t plan;  // from the lengths in the host copy of the input
+    rc = pkv_plan(pr, host_lens(sb), num_sms, policy, &plan);
     if (rc != PKV_OK) return rc;
     if ((int64_t)ws_bytes < plan.ws_bytes) return PKV_E_WS_TOO_SMALL;
     if (plan_out) *plan_out = plan;
-    char* d = static_cast<char*>(dev_in);
-    // Page-locked host buffers mapped into the device's address space are read and written by kernels directly
-    // (the input by a copy kernel, out by the step's own output stores); others go through cudaMemcpyAsync.
-    const void* in_mapped = mapped_host_address(host_in);
-    void* out_mapped = const_cast<void*>(mapped_host_address(host_out));
-    void* out = out_mapped ? out_mapped : dev_out;
-    rc = check_decode_args(&plan, pr, d + off[0], k_pool, v_pool, reinterpret_cast<const int32_t*>(d + off[3]),
-                           reinterpret_cast<const int32_t*>(d + off[4]), scale, ws, ws_bytes, out);
+    rc = check_serve(sb, &plan);
     if (rc != PKV_OK) return rc;
-    if (pr->batch == 0) return PKV_OK;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (in_mapped) {
-        if (launch_stage_copy(in_mapped, dev_in, total, stream) != cudaSuccess) return PKV_E_CUDA;
-    } else if (cudaMemcpyAsync(dev_in, host_in, total, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    return serve_enqueue(sb, &plan, static_cast<cudaStream_t>(stream));
+}
+
+// A serving session: the buffers bound once, and every distinct plan's launches captured once into a CUDA graph
+// (on a private stream) that later steps with the same plan replay with one cudaGraphLaunch.
+struct pkv_session {
+    ServeBind sb;
+    pkv_policy pol;
+    bool have_pol;
+    int32_t num_sms;
+    bool graphs;             // both host buffers are mapped: the step is kernels only and can be captured
+    cudaStream_t capture;    // private stream the graphs are captured on
+    struct Entry {
+        pkv_plan_t key;      // the plan without its lens-dependent estimates (predicted_us, kv_bytes)
+        cudaGraphExec_t exec;
+        uint64_t used;
+    };
+    Entry cache[PKV_SESSION_GRAPHS];
+    int n;
+    uint64_t clock;
+    int64_t captured, replayed;
+};
+
+extern "C" int pkv_session_create(const pkv_problem* pr, const pkv_policy* policy, int32_t num_sms,
+                                  const void* host_in, void* dev_in, void* k_pool, void* v_pool, float scale, void* ws,
+                                  size_t ws_bytes, void* dev_out, void* host_out, pkv_session** session) {
+    if (!session) return PKV_E_NULLPTR;
+    *session = nullptr;
+    if (num_sms <= 0) return PKV_E_INVAL;
+    ServeBind sb;
+    int rc = bind_serve(pr, host_in, dev_in, k_pool, v_pool, scale, ws, ws_bytes, dev_out, host_out, &sb);
+    if (rc != PKV_OK) return rc;
+    pkv_session* s = new (std::nothrow) pkv_session();
+    if (!s) return PKV_E_CUDA;
+    s->sb = sb;
+    s->have_pol = policy != nullptr;
+    if (policy) s->pol = *policy;
+    s->num_sms = num_sms;
+    s->graphs = sb.pr.batch > 0 && sb.in_mapped != nullptr && sb.out_mapped != nullptr;
+    s->capture = nullptr;
+    if (s->graphs && cudaStreamCreateWithFlags(&s->capture, cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        delete s;
         return PKV_E_CUDA;
     }
-    rc = decode_step(&plan, pr, d + off[0], d + off[1], d + off[2], k_pool, v_pool,
-                     reinterpret_cast<const int32_t*>(d + off[3]), reinterpret_cast<const int32_t*>(d + off[4]), scale,
-                     ws, ws_bytes, out, stream, false);
-    if (rc != PKV_OK) return rc;
-    const size_t out_bytes = (size_t)pr->batch * pr->num_q_heads * pr->head_dim * 2;
-    if (!out_mapped && cudaMemcpyAsync(host_out, dev_out, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return PKV_E_CUDA;
+    *session = s;
     return PKV_OK;
+}
+
+extern "C" int pkv_session_step(pkv_session* s, void* stream, pkv_plan_t* plan_out) {
+    if (!s) return PKV_E_NULLPTR;
+    const ServeBind& sb = s->sb;
+    pkv_plan_t plan;
+    int rc = pkv_plan(&sb.pr, host_lens(sb), s->num_sms, s->have_pol ? &s->pol : nullptr, &plan);
+    if (rc != PKV_OK) return rc;
+    if (plan_out) *plan_out = plan;
+    rc = check_serve(sb, &plan);
+    if (rc != PKV_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    bool graph = s->graphs;
+    if (graph) {  // a stream the caller is capturing gets the launches themselves
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+            cudaGetLastError();
+            graph = false;
+        } else if (cs != cudaStreamCaptureStatusNone) {
+            graph = false;
+        }
+    }
+    if (!graph) return serve_enqueue(sb, &plan, st);
+    pkv_plan_t key = plan;
+    key.predicted_us = 0.0;
+    key.kv_bytes = 0.0;
+    for (int i = 0; i < s->n; ++i) {
+        if (std::memcmp(&s->cache[i].key, &key, sizeof(key)) == 0) {
+            s->cache[i].used = ++s->clock;
+            if (cudaGraphLaunch(s->cache[i].exec, st) != cudaSuccess) return PKV_E_CUDA;
+            ++s->replayed;
+            return PKV_OK;
+        }
+    }
+    if (cudaStreamBeginCapture(s->capture, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_E_CUDA;
+    }
+    rc = serve_enqueue(sb, &plan, s->capture);
+    cudaGraph_t g = nullptr;
+    const cudaError_t end = cudaStreamEndCapture(s->capture, &g);
+    cudaGraphExec_t exec = nullptr;
+    if (rc == PKV_OK && (end != cudaSuccess || !g || cudaGraphInstantiate(&exec, g, 0) != cudaSuccess)) rc = PKV_E_CUDA;
+    if (g) cudaGraphDestroy(g);
+    if (rc != PKV_OK) {
+        cudaGetLastError();
+        return rc;
+    }
+    int slot = s->n;
+    if (s->n == PKV_SESSION_GRAPHS) {  // the least recently used graph makes room
+        slot = 0;
+        for (int i = 1; i < s->n; ++i)
+            if (s->cache[i].used < s->cache[slot].used) slot = i;
+        cudaGraphExecDestroy(s->cache[slot].exec);
+    } else {
+        ++s->n;
+    }
+    s->cache[slot].key = key;
+    s->cache[slot].exec = exec;
+    s->cache[slot].used = ++s->clock;
+    ++s->captured;
+    if (cudaGraphLaunch(exec, st) != cudaSuccess) return PKV_E_CUDA;
+    ++s->replayed;
+    return PKV_OK;
+}
+
+extern "C" int pkv_session_stats(const pkv_session* s, int64_t* graphs_captured, int64_t* graph_launches) {
+    if (!s || !graphs_captured || !graph_launches) return PKV_E_NULLPTR;
+    *graphs_captured = s->captured;
+    *graph_launches = s->replayed;
+    return PKV_OK;
+}
+
+extern "C" int pkv_session_destroy(pkv_session* s) {
+    if (!s) return PKV_OK;
+    int rc = PKV_OK;
+    for (int i = 0; i < s->n; ++i)
+        if (cudaGraphExecDestroy(s->cache[i].exec) != cudaSuccess) rc = PKV_E_CUDA;
+    if (s->capture && cudaStreamDestroy(s->capture) != cudaSuccess) rc = PKV_E_CUDA;
+    if (rc != PKV_OK) cudaGetLastError();
+    delete s;
+    return rc;
 }
 
 extern "C" int pkv_read_status(void* ws, size_t ws_bytes, void* stream, uint32_t* status) {

@@ -11,7 +11,6 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
-#include <vector>
 
 #include "pkv_internal.h"
 #include "policy_constants.h"
@@ -139,60 +138,75 @@ int fill_plan(const pkv_problem* pr, const int32_t* lens, int32_t num_sms, int32
     return PKV_OK;
 }
 
-// Step time of a plan under the model documented with pkv_policy (include/pkv.h).
-double predict_us(const pkv_policy* pol, const pkv_plan_t* plan, const int32_t* lens) {
-    const pkv_problem& pr = plan->problem;
-    const int B = pr.batch, G = plan->group;
-    const double T = plan->num_tasks;
-    if (T <= 0) return pol->launch_us;
-    const double W = (double)std::max(1, plan->grid_ctas);
-    const double A = std::min(T, W);
+// What the model needs of a candidate plan (the rest of pkv_plan_t is workspace layout).
+struct Cand {
+    int32_t variant, chunk, group, list_in_decode, fuse;
+    int64_t splits, tasks, grid, p_max;
+    double kv_bytes;
+};
+
+int64_t max_row_pages(const int32_t* lens, int B) {
     int64_t p_max = 0;
     for (int b = 0; b < B; ++b) p_max = std::max<int64_t>(p_max, ((int64_t)lens[b] + kPageSize - 1) / kPageSize);
-    const double pages_per_task = plan->variant == PKV_VARIANT_SINGLE ? (double)p_max
-                                                                       : (double)std::min<int64_t>(plan->chunk_pages, p_max);
+    return p_max;
+}
+
+Cand cand_of(const pkv_plan_t* plan, const int32_t* lens) {
+    Cand c;
+    c.variant = plan->variant;
+    c.chunk = plan->chunk_pages;
+    c.group = plan->group;
+    c.list_in_decode = plan->list_in_decode;
+    c.fuse = plan->fuse_merge;
+    c.splits = plan->num_splits;
+    c.tasks = plan->num_tasks;
+    c.grid = plan->grid_ctas;
+    c.p_max = max_row_pages(lens, plan->problem.batch);
+    c.kv_bytes = plan->kv_bytes;
+    return c;
+}
+
+// Step time of a candidate under the model documented with pkv_policy (include/pkv.h).
+double predict(const pkv_policy* pol, const Cand& c) {
+    const double T = (double)c.tasks;
+    if (T <= 0) return pol->launch_us;
+    const double W = (double)std::max<int64_t>(1, c.grid);
+    const double A = std::min(T, W);
+    const double pages_per_task = c.variant == PKV_VARIANT_SINGLE ? (double)c.p_max
+                                                                   : (double)std::min<int64_t>(c.chunk, c.p_max);
     const double task_bytes = pages_per_task * kPageSize * kTokenHeadBytes;
     const double gb = 1e3;  // bytes / (GB/s * 1e3) = microseconds
     double t;
-    if (plan->variant == PKV_VARIANT_WORKQUEUE) {
-        const double stream = plan->kv_bytes / (std::min(pol->hbm_gbs, A * pol->wq_cta_gbs) * gb);
+    if (c.variant == PKV_VARIANT_WORKQUEUE) {
+        const double stream = c.kv_bytes / (std::min(pol->hbm_gbs, A * pol->wq_cta_gbs) * gb);
         const double makespan = std::ceil(T / W) * task_bytes / (pol->wq_cta_gbs * gb);
         t = pol->launch_us + stream + (T / W) * pol->task_us + pol->tail * std::max(0.0, makespan - stream);
     } else {
         const double share = std::min(pol->cta_gbs, pol->hbm_gbs / A) * gb;
-        t = pol->launch_us + std::ceil(T / W) * (pol->task_us + (plan->kv_bytes / T) / share);
+        t = pol->launch_us + std::ceil(T / W) * (pol->task_us + (c.kv_bytes / T) / share);
     }
-    if (plan->variant != PKV_VARIANT_SINGLE) {
-        const double s_max = plan->variant == PKV_VARIANT_SPLIT
-                                 ? (double)plan->num_splits
-                                 : std::ceil((double)p_max / std::max(1, plan->chunk_pages));
-        if (plan->fuse_merge)
-            t += pol->fused_us + pol->fused_state_us * s_max * G;
+    if (c.variant != PKV_VARIANT_SINGLE) {
+        const double s_max = c.variant == PKV_VARIANT_SPLIT ? (double)c.splits
+                                                            : std::ceil((double)c.p_max / std::max(1, c.chunk));
+        if (c.fuse)
+            t += pol->fused_us + pol->fused_state_us * s_max * c.group;
         else
             t += pol->merge_us + pol->merge_state_us * s_max;
     }
-    if (plan->variant == PKV_VARIANT_WORKQUEUE && !plan->list_in_decode) t += pol->build_us;
+    if (c.variant == PKV_VARIANT_WORKQUEUE && !c.list_in_decode) t += pol->build_us;
     return t;
 }
 
-// Picks the cheaper merge mode for a split or workqueue plan (the fused one only if allowed).
-void choose_merge(const pkv_policy* pol, pkv_plan_t* plan, const int32_t* lens) {
-    if (plan->variant == PKV_VARIANT_SINGLE) {
-        plan->fuse_merge = 0;
-        plan->predicted_us = predict_us(pol, plan, lens);
-        return;
-    }
-    plan->fuse_merge = 0;
-    const double sep = predict_us(pol, plan, lens);
-    plan->predicted_us = sep;
-    if (pol->allow_fused) {
-        plan->fuse_merge = 1;
-        const double fused = predict_us(pol, plan, lens);
-        if (fused < sep)
-            plan->predicted_us = fused;
-        else
-            plan->fuse_merge = 0;
-    }
+// The cheaper merge mode for a candidate (the fused one only if allowed and not single pass); returns its time.
+double choose_merge(const pkv_policy* pol, Cand& c) {
+    c.fuse = 0;
+    const double sep = predict(pol, c);
+    if (c.variant == PKV_VARIANT_SINGLE || !pol->allow_fused) return sep;
+    c.fuse = 1;
+    const double fused = predict(pol, c);
+    if (fused < sep) return fused;
+    c.fuse = 0;
+    return sep;
 }
 
 }  // namespace
@@ -203,7 +217,9 @@ extern "C" int pkv_plan_fixed(const pkv_problem* pr, const int32_t* lens, int32_
     if (rc != PKV_OK) return rc;
     pkv_policy pol;
     pkv_policy_default(&pol);
-    choose_merge(&pol, plan, lens);
+    Cand c = cand_of(plan, lens);
+    plan->predicted_us = choose_merge(&pol, c);
+    plan->fuse_merge = c.fuse;
     return PKV_OK;
 }
 
@@ -220,37 +236,74 @@ extern "C" int pkv_plan(const pkv_problem* pr, const int32_t* lens, int32_t num_
     if (pol.ctas_per_sm <= 0 || pol.max_splits <= 0 || !(pol.hbm_gbs > 0) || !(pol.cta_gbs > 0) ||
         !(pol.wq_cta_gbs > 0))
         return PKV_E_INVAL;
-    int64_t max_pages = 0;
-    for (int b = 0; b < pr->batch; ++b) {
-        if (lens[b] < 0) return PKV_E_INVAL;
+    if (num_sms <= 0) return PKV_E_INVAL;
+    const int B = pr->batch, Hkv = pr->num_kv_heads, G = pr->num_q_heads / pr->num_kv_heads;
+    int64_t max_pages = 0, sum_len = 0;
+    for (int b = 0; b < B; ++b) {
+        if (lens[b] < 0 || (int64_t)lens[b] > (int64_t)pr->max_pages_per_seq * kPageSize) return PKV_E_INVAL;
         max_pages = std::max<int64_t>(max_pages, (lens[b] + kPageSize - 1) / kPageSize);
+        sum_len += lens[b];
     }
+    // the grid limit fill_plan applies: CTAs per SM within registers and shared memory
+    int ctas_per_sm = std::min<int>(pol.ctas_per_sm, kDecodeCtasPerSm);
+    const int smem = decode_smem_bytes(G);
+    if (smem > 0) ctas_per_sm = std::max(1, std::min(ctas_per_sm, kSmemPerSm / (smem + kSmemReservedPerCta)));
+    const int64_t grid_cap = (int64_t)ctas_per_sm * num_sms;
     // candidate split sizes: powers of two and 1.5x powers of two, bounded so that S <= max_splits
-    std::vector<int32_t> chunks;
+    int32_t chunks[128];
+    int nchunks = 0;
     const int64_t cmin = std::max<int64_t>(1, (max_pages + pol.max_splits - 1) / pol.max_splits);
-    for (int64_t c = 1; c <= std::max<int64_t>(1, max_pages); c *= 2) {
-        if (c >= cmin) chunks.push_back((int32_t)c);
+    for (int64_t c = 1; c <= std::max<int64_t>(1, max_pages) && nchunks < 126; c *= 2) {
+        if (c >= cmin) chunks[nchunks++] = (int32_t)c;
         const int64_t c3 = c + c / 2;
-        if (c3 > c && c3 >= cmin && c3 <= max_pages) chunks.push_back((int32_t)c3);
+        if (c3 > c && c3 >= cmin && c3 <= max_pages) chunks[nchunks++] = (int32_t)c3;
     }
-    if (chunks.empty()) chunks.push_back((int32_t)std::max<int64_t>(1, cmin));
+    if (nchunks == 0) chunks[nchunks++] = (int32_t)std::max<int64_t>(1, cmin);
+    // every candidate is scored on the few numbers the model reads; only the winner's workspace layout is filled
+    const double kv_bytes = (double)kTokenHeadBytes * Hkv * (double)sum_len + 2.0 * 2.0 * (double)B * pr->num_q_heads * kHeadDim;
     bool have = false;
-    pkv_plan_t best{}, cand{};
+    Cand best{};
+    double best_us = 0.0;
     for (int v = PKV_VARIANT_SINGLE; v <= PKV_VARIANT_WORKQUEUE; ++v) {
         if (!(pol.allow_variants & (1 << v))) continue;
-        if (v == PKV_VARIANT_SPLIT && pr->batch > pol.split_max_batch) continue;
-        const size_t n = v == PKV_VARIANT_SINGLE ? 1 : chunks.size();
-        for (size_t i = 0; i < n; ++i) {
-            if (fill_plan(pr, lens, num_sms, v, chunks[i], pol.ctas_per_sm, &cand) != PKV_OK) continue;
-            choose_merge(&pol, &cand, lens);
-            if (!have || cand.predicted_us < best.predicted_us) {
-                best = cand;
+        if (v == PKV_VARIANT_SPLIT && B > pol.split_max_batch) continue;
+        const int n = v == PKV_VARIANT_SINGLE ? 1 : nchunks;
+        for (int i = 0; i < n; ++i) {
+            const int32_t chunk = v == PKV_VARIANT_SINGLE ? std::max<int32_t>(1, pr->max_pages_per_seq) : chunks[i];
+            int64_t splits = 0, wq_tasks = 0;
+            for (int b = 0; b < B; ++b) {
+                const int64_t S = (((int64_t)lens[b] + kPageSize - 1) / kPageSize + chunk - 1) / chunk;
+                splits = std::max(splits, S);
+                wq_tasks += (int64_t)Hkv * S;
+            }
+            if (v == PKV_VARIANT_SINGLE) splits = 1;
+            if (splits > 0xffff) continue;
+            splits = std::max<int64_t>(splits, 1);
+            const int64_t tasks = v == PKV_VARIANT_WORKQUEUE ? wq_tasks : (int64_t)B * Hkv * splits;
+            if (tasks > 0x7fffffffLL / G) continue;
+            Cand c;
+            c.variant = v;
+            c.chunk = chunk;
+            c.group = G;
+            c.list_in_decode = v == PKV_VARIANT_WORKQUEUE && B <= PKV_MAX_ROWS_IN_DECODE ? 1 : 0;
+            c.splits = splits;
+            c.tasks = tasks;
+            c.grid = std::max<int64_t>(1, std::min<int64_t>(tasks, grid_cap));
+            c.p_max = max_pages;
+            c.kv_bytes = kv_bytes;
+            const double us = choose_merge(&pol, c);
+            if (!have || us < best_us) {
+                best = c;
+                best_us = us;
                 have = true;
             }
         }
     }
     if (!have) return PKV_E_INVAL;
-    *plan = best;
+    rc = fill_plan(pr, lens, num_sms, best.variant, best.chunk, pol.ctas_per_sm, plan);
+    if (rc != PKV_OK) return rc;
+    plan->fuse_merge = best.fuse;
+    plan->predicted_us = best_us;
     return PKV_OK;
 }
 

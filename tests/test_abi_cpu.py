@@ -204,3 +204,33 @@ def test_serve_step_rejects_missing_buffers_before_any_work():
     rc = lib.pkv_serve_step(ctypes.byref(pr), None, 152, None, None, None, None, ctypes.c_float(0.1), None, 0, None,
                             None, None, ctypes.byref(plan))
     assert rc == -3  # PKV_E_NULLPTR
+
+
+def test_session_rejects_bad_arguments_before_any_work():
+    """pkv_session_create / _step / _stats / _destroy: error codes for missing or misaligned buffers, a missing
+    handle and a non-positive SM count, with nothing created (the handle stays NULL) and no device call."""
+    lib = pkv.load()
+    pr = pkv.make_problem(1, 32, 8, 128, 16, 64, 32)
+    h = ctypes.c_void_p(1)
+    f32 = ctypes.c_float(0.1)
+    vp = ctypes.c_void_p
+    a256, a16 = vp(1 << 20), vp((1 << 20) + 16)  # aligned stand-ins, never dereferenced: validation fails first
+    assert lib.pkv_session_create(ctypes.byref(pr), None, 152, None, a256, a256, a256, f32, a256, 1 << 20, a256,
+                                  a256, ctypes.byref(h)) == -3  # PKV_E_NULLPTR (host_in)
+    assert h.value is None
+    assert lib.pkv_session_create(ctypes.byref(pr), None, 152, a256, a16, a256, a256, f32, a256, 1 << 20, a256,
+                                  a256, ctypes.byref(h)) == -5  # PKV_E_ALIGN (dev_in not 256-byte aligned)
+    assert lib.pkv_session_create(ctypes.byref(pr), None, 152, vp((1 << 20) + 8), a256, a256, a256, f32, a256,
+                                  1 << 20, a256, a256, ctypes.byref(h)) == -5  # host_in not 16-byte aligned
+    assert lib.pkv_session_create(ctypes.byref(pr), None, 0, a256, a256, a256, a256, f32, a256, 1 << 20, a256,
+                                  a256, ctypes.byref(h)) == -1  # PKV_E_INVAL (num_sms)
+    assert lib.pkv_session_create(ctypes.byref(pr), None, 152, a256, a256, a256, a256, f32, a256, 1 << 20, a256,
+                                  a256, None) == -3
+    bad = pkv.make_problem(1, 32, 8, 64, 16, 64, 32)  # d = 64
+    assert lib.pkv_session_create(ctypes.byref(bad), None, 152, a256, a256, a256, a256, f32, a256, 1 << 20, a256,
+                                  a256, ctypes.byref(h)) == -2  # PKV_E_UNSUPPORTED
+    plan = pkv.Plan()
+    assert lib.pkv_session_step(None, None, ctypes.byref(plan)) == -3
+    n1, n2 = ctypes.c_int64(), ctypes.c_int64()
+    assert lib.pkv_session_stats(None, ctypes.byref(n1), ctypes.byref(n2)) == -3
+    assert lib.pkv_session_destroy(None) == 0

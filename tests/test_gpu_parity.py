@@ -535,3 +535,103 @@ def test_overlapping_layers_read_the_previous_layers_output(name, seed, t, varia
         q_in = bufs[layer].cpu().numpy()
         ref = oracle.attention(q_in, kp, vp, step.bt_host, step.lens_host, step.scale)
         assert_close(bufs[layer + 1], ref, f"{name} layer {layer} variant {variant} fused {fused}")
+
+
+# ------------------------------------------------------------------------------------------------ serving session
+def _pack_step(problem, host_in, q, k_new, v_new, bt, lens):
+    offs, _ = pkv.pkv_step_input_layout(problem)
+    for i, part in enumerate((q, k_new, v_new, bt, lens)):
+        raw = torch.as_tensor(np.ascontiguousarray(part)).view(torch.uint8).reshape(-1)
+        host_in[offs[i]:offs[i] + raw.numel()] = raw
+
+
+def _launch_key(plan):
+    return tuple(getattr(plan, f) for f, _ in plan._fields_ if f not in ("predicted_us", "kv_bytes", "problem"))
+
+
+def _session_loop(session, base, tr, kp, vp, host_in, host_out, steps, lens_of, bt_of, q_of=None):
+    """Runs the session over `steps`; for each, the new token's pool slots are poisoned first and must hold its K/V
+    afterwards, and out must match the oracle. Returns the plans."""
+    B = tr.batch
+    q_of = tr.q if q_of is None else q_of
+    plans = []
+    for t in steps:
+        lens, bt, q = lens_of(t), bt_of(t), q_of(t)
+        rows = np.arange(B)
+        phys = bt[rows, (lens - 1) // tr.ps]
+        slot = (lens - 1) % tr.ps
+        k_new, v_new = kp[phys, slot], vp[phys, slot]
+        pi, si = torch.from_numpy(phys.astype(np.int64)).cuda(), torch.from_numpy(slot.astype(np.int64)).cuda()
+        base.k[pi, si] = float("nan")
+        base.v[pi, si] = float("nan")
+        _pack_step(base.problem, host_in, q, k_new, v_new, bt, lens)
+        host_out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        plan = session.run()
+        torch.cuda.synchronize()
+        plans.append(_launch_key(plan))
+        ref = oracle.attention(q, kp, vp, bt, lens, base.scale)
+        assert_close(host_out.cuda(), ref, f"session step t={t} lens={lens[:4]}")
+        assert torch.equal(base.k[pi, si].cpu(), torch.from_numpy(k_new)), "new K not appended"
+        assert torch.equal(base.v[pi, si].cpu(), torch.from_numpy(v_new)), "new V not appended"
+    return plans
+
+
+@pytest.mark.parametrize("name,seed,t0,n", [("b1_bucketed", 5, 0, 4), ("b8_bimodal", 6, 0, 6),
+                                            ("b4_bimodal", 5, 10, 4), ("tiny", 1, 0, 3)])
+def test_serve_session_decode_loop_replays_graphs(name, seed, t0, n):
+    """A decode loop through one ServeSession (buffers bound once, host_in refilled every step): every step matches
+    the oracle and appends its token; the session captures one CUDA graph per distinct plan and launches a graph on
+    every step. With pageable host buffers it enqueues the launches directly (no graph) and still matches."""
+    tr = make_trace(name, seed, steps=t0 + n)
+    base = Step(tr, t0, poison=False)
+    kp, vp = tr.host_pools()
+    B, Hq, d = tr.batch, tr.hq, tr.d
+    steps = list(range(t0, t0 + n))
+    ws_bytes = max(pkv.pkv_plan(base.problem, tr.seq_lens(t), base.sms).ws_bytes for t in steps)
+    ws = pkv.alloc_workspace(ws_bytes)
+    _, total = pkv.pkv_step_input_layout(base.problem)
+    dev_in = torch.empty(total, dtype=torch.uint8, device="cuda")
+    dev_out = torch.empty((B, Hq, d), dtype=torch.float16, device="cuda")
+    host_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    host_out = torch.empty((B, Hq, d), dtype=torch.float16).pin_memory()
+    session = pkv.ServeSession(base.problem, host_in, dev_in, base.k, base.v, base.scale, ws, dev_out, host_out)
+    plans = _session_loop(session, base, tr, kp, vp, host_in, host_out, steps, tr.seq_lens, tr.block_table)
+    assert session.stats() == (len(set(plans)), n), (session.stats(), len(set(plans)))
+    assert pkv.pkv_read_status(ws) == 0
+    session.close()
+    # pageable host buffers: no graph
+    pin = torch.zeros(total, dtype=torch.uint8)
+    pout = torch.empty((B, Hq, d), dtype=torch.float16)
+    direct = pkv.ServeSession(base.problem, pin, dev_in, base.k, base.v, base.scale, ws, dev_out, pout)
+    _session_loop(direct, base, tr, kp, vp, pin, pout, steps[:2], tr.seq_lens, tr.block_table)
+    assert direct.stats() == (0, 0)
+    direct.close()
+
+
+def test_serve_session_evicts_the_least_recently_used_graph():
+    """More distinct plans than the session keeps graphs for (B = 1 rows cut to 18 lengths, each a different split
+    count): every step matches the oracle; the 17th and 18th plans evict the two oldest graphs, so rerunning the
+    first length captures again while rerunning the last one replays."""
+    tr = make_trace("b1_bucketed", 5, steps=1)
+    base = Step(tr, 0, poison=False)
+    kp, vp = tr.host_pools()
+    L0 = int(tr.seq_lens(0)[0])
+    cut = [np.array([L0 - 130 * k], dtype=np.int32) for k in range(pkv.PKV_SESSION_GRAPHS + 2)]
+    plans = [pkv.pkv_plan(base.problem, c, base.sms) for c in cut]
+    assert len({_launch_key(p) for p in plans}) == len(cut)
+    ws = pkv.alloc_workspace(max(p.ws_bytes for p in plans))
+    _, total = pkv.pkv_step_input_layout(base.problem)
+    dev_in = torch.empty(total, dtype=torch.uint8, device="cuda")
+    dev_out = torch.empty((1, tr.hq, tr.d), dtype=torch.float16, device="cuda")
+    host_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    host_out = torch.empty((1, tr.hq, tr.d), dtype=torch.float16).pin_memory()
+    session = pkv.ServeSession(base.problem, host_in, dev_in, base.k, base.v, base.scale, ws, dev_out, host_out)
+    bt = tr.block_table(0)
+    order = list(range(len(cut))) + [0, len(cut) - 1]
+    _session_loop(session, base, tr, kp, vp, host_in, host_out, order, lambda i: cut[i], lambda i: bt,
+                  lambda i: tr.q(0))
+    n = len(cut)
+    assert session.stats() == (n + 1, n + 2)
+    assert pkv.pkv_read_status(ws) == 0
+    session.close()
