@@ -242,10 +242,14 @@ class ServeSession:
         self._streams = {}
 
     def run(self, stream=None) -> Plan:
-        key = id(stream)
-        args = self._streams.get(key)
-        if args is None:
-            args = self._streams[key] = (self._h, _stream(stream), ctypes.byref(self.plan))
+        """One step on `stream` (None: the current stream, looked up on every call)."""
+        if stream is None:
+            args = (self._h, _stream(None), ctypes.byref(self.plan))
+        else:
+            hit = self._streams.get(id(stream))
+            if hit is None or hit[0] is not stream:  # the stream object is kept, so its id cannot be reused
+                hit = self._streams[id(stream)] = (stream, (self._h, _stream(stream), ctypes.byref(self.plan)))
+            args = hit[1]
         rc = self._lib.pkv_session_step(*args)
         if rc != 0:
             check(rc, "pkv_session_step")
