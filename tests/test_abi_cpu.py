@@ -234,3 +234,22 @@ def test_session_rejects_bad_arguments_before_any_work():
     n1, n2 = ctypes.c_int64(), ctypes.c_int64()
     assert lib.pkv_session_stats(None, ctypes.byref(n1), ctypes.byref(n2)) == -3
     assert lib.pkv_session_destroy(None) == 0
+
+
+def test_session_with_an_empty_batch_runs_without_the_device():
+    """A B = 0 session: create, a step (the plan has no task, nothing is enqueued), stats and destroy all succeed
+    with no device work, and no graph is captured."""
+    lib = pkv.load()
+    pr = pkv.make_problem(0, 32, 8, 128, 16, 64, 32)
+    vp = ctypes.c_void_p
+    a256 = vp(1 << 20)  # aligned stand-ins: with no rows nothing is read or written
+    h = vp()
+    assert lib.pkv_session_create(ctypes.byref(pr), None, 152, a256, a256, a256, a256, ctypes.c_float(0.1), a256,
+                                  1 << 20, a256, a256, ctypes.byref(h)) == 0
+    plan = pkv.Plan()
+    assert lib.pkv_session_step(h, None, ctypes.byref(plan)) == 0
+    assert plan.num_tasks == 0
+    n1, n2 = ctypes.c_int64(-1), ctypes.c_int64(-1)
+    assert lib.pkv_session_stats(h, ctypes.byref(n1), ctypes.byref(n2)) == 0
+    assert (n1.value, n2.value) == (0, 0)
+    assert lib.pkv_session_destroy(h) == 0
