@@ -1,5 +1,5 @@
-// Persistent split-KV paged GQA decode kernel for sm_103a, with the log-sum-exp merge fused into the last task of
-// every (row, KV head).
+// Persistent split-KV paged GQA decode kernel for sm_103a; optionally with the log-sum-exp merge of the split states
+// fused in (run by the CTA whose task of a (row, KV head) finishes last).
 //
 // Computes, for every task (row b, KV head h, logical pages [page_begin, page_end)), the online-softmax state of
 // the G = Hq/Hkv query heads that share KV head h ("PersistentKV: Page-Aware Decode Scheduling for Long-Context LLM
@@ -9,17 +9,20 @@
 // neutral states for empty splits ("Row-Local Bounds"), compact workqueue ("Compact Workqueue")).
 //
 // CTA layout (persistent over tasks; grid = one wave of resident CTAs):
-//   warp NCW+2  scheduler: takes tasks (split / single: a static stride over the (b, h, s) task space; workqueue: an
-//               atomic queue head over the built list in the same order,
-//               after waiting for the builder grid), bulk-copies the G query rows of the task into a shared-memory
+//   warp NCW+2  scheduler: takes tasks (split / single: a static stride over the (b, h, s) task space; workqueue:
+//               task blockIdx.x first, then an atomic queue head; a list the decode derives itself from seq_lens is
+//               claimed split by split within a row (the KV heads of one split, which read the same pages, one after
+//               the other), a list written by the worklist builder in its order, after waiting for the builder
+//               grid), bulk-copies the G query rows of the task into a shared-memory
 //               task slot (completion on their own barrier), fetches the row length and the task's first 32
 //               block-table entries together and publishes them in the slot. With the merge fused it also publishes
 //               merge tasks that the epilogue warp requests, and ends only after the epilogue has seen every task;
 //   warp NCW+1  loader: per page, one elected lane issues four 3-D TMA tensor copies (K and V of KV head h, each as
 //               two 64-column boxes of the page's 16 token rows, 128-byte swizzled) into a ring stage, counted in
-//               bytes on the stage's mbarrier; block-table entries past the slot's 32 are read one chunk ahead. For a
-//               static plan it reads its first task's entries itself before the CTA barrier. A merge task's partial
-//               states go through the same ring, 16 states (8 KB of acc) per stage, by bulk copies;
+//               bytes on the stage's mbarrier; block-table entries past the slot's 32 are read one chunk ahead. When
+//               the CTA's first task is known before the CTA barrier (static plans, and a workqueue derived in the
+//               decode) it reads that task's entries itself and issues its first page copies at once. A merge
+//               task's partial states go through the same ring, 16 states (8 KB of acc) per stage, by bulk copies;
 //   warps 0..NCW-1 consumers: page j of the CTA's page sequence (counted across tasks) lives in stage j % NS and
 //               goes to warp j % NCW (NS % NCW == 0, so a stage always has the same consumer). The products are
 //               taken transposed, so the 16 tokens (scores) and the head dimension (output) fill the 16-row side of
