@@ -185,6 +185,16 @@ typedef struct pkv_ws_header {
  */
 #define PKV_PLAN_OVERLAP_PREV 0x1u
 
+/*
+ * Plan flag: the step may start while the kernel enqueued just before it on the same stream is still running, and
+ * that kernel may write every input (q, k_new, v_new, block_table, seq_lens; e.g. the copy of the step's packed
+ * input into device memory): the CTAs only set up their shared memory and barriers before griddepcontrol.wait and
+ * read nothing until that kernel has completed. Takes precedence over PKV_PLAN_OVERLAP_PREV. Ignored by plans that
+ * run the worklist builder. pkv_serve_step and the serving session set it on the decode that follows their input
+ * copy kernel.
+ */
+#define PKV_PLAN_INPUTS_AFTER_PREV 0x2u
+
 /* Library version (PKV_VERSION). */
 int pkv_version(void);
 

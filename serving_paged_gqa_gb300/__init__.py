@@ -5,7 +5,8 @@ sequence split, compact device-built workqueue), a log-sum-exp merge, a device w
 roofline cost-model planner, all in libpkv.so (C ABI: include/pkv.h). This package is its Python binding.
 """
 
-from ._lib import (EXPORTS, LIB_PATH, PKV_MAX_BATCH, PKV_MAX_ROWS_IN_DECODE, PKV_PLAN_OVERLAP_PREV,  # noqa: F401
+from ._lib import (EXPORTS, LIB_PATH, PKV_MAX_BATCH, PKV_MAX_ROWS_IN_DECODE, PKV_PLAN_INPUTS_AFTER_PREV,  # noqa: F401
+                   PKV_PLAN_OVERLAP_PREV,
                    PKV_SESSION_GRAPHS, PKV_STATIC_SCRATCH_BYTES,
                    PKV_STATUS_BAD_LEN, PKV_STATUS_BAD_PAGE, PKV_STATUS_TASKS, PKV_STATUS_TIMEOUT, PKV_VARIANT_SINGLE,
                    PKV_VARIANT_SPLIT, PKV_VARIANT_WORKQUEUE, VARIANT_NAMES, PkvError, load)

@@ -29,6 +29,7 @@ PKV_MAX_BATCH = 4096
 PKV_MAX_ROWS_IN_DECODE = 256
 
 PKV_PLAN_OVERLAP_PREV = 0x1
+PKV_PLAN_INPUTS_AFTER_PREV = 0x2
 
 PKV_VARIANT_SINGLE = 0
 PKV_VARIANT_SPLIT = 1

@@ -28,7 +28,7 @@ int check_plan(const pkv_plan_t* plan, const pkv_problem* pr, const void* ws, si
         (plan->list_in_decode != 0 && plan->list_in_decode != 1))
         return PKV_E_INVAL;
     if (plan->list_in_decode && pr->batch > PKV_MAX_ROWS_IN_DECODE) return PKV_E_UNSUPPORTED;
-    if ((uint32_t)plan->flags & ~PKV_PLAN_OVERLAP_PREV) return PKV_E_INVAL;
+    if ((uint32_t)plan->flags & ~(PKV_PLAN_OVERLAP_PREV | PKV_PLAN_INPUTS_AFTER_PREV)) return PKV_E_INVAL;
     if (plan->off_counters < (int64_t)sizeof(pkv_ws_header) ||
         plan->off_counters + 4 * (int64_t)pr->batch * pr->num_kv_heads > plan->ws_bytes)
         return PKV_E_INVAL;
@@ -245,8 +245,10 @@ int pkv::decode_launch(const pkv_plan_t* plan, const pkv_problem* pr, const void
     // only after griddepcontrol.wait). Otherwise it may start early only if the plan says the kernel before it writes
     // none of what the decode reads before that wait.
     const bool builder = plan->variant == PKV_VARIANT_WORKQUEUE && !plan->list_in_decode;
-    const bool pdl = builder || ((uint32_t)plan->flags & PKV_PLAN_OVERLAP_PREV);
-    p.overlap_prev = !builder && ((uint32_t)plan->flags & PKV_PLAN_OVERLAP_PREV) ? 1 : 0;
+    const uint32_t flags = (uint32_t)plan->flags;
+    const bool pdl = builder || (flags & (PKV_PLAN_OVERLAP_PREV | PKV_PLAN_INPUTS_AFTER_PREV));
+    p.inputs_after_wait = !builder && (flags & PKV_PLAN_INPUTS_AFTER_PREV) ? 1 : 0;
+    p.overlap_prev = !builder && !p.inputs_after_wait && (flags & PKV_PLAN_OVERLAP_PREV) ? 1 : 0;
     return cuda_rc(launch_decode(p, plan->group, plan->grid_ctas, pdl, stream));
 }
 
@@ -379,12 +381,14 @@ int serve_enqueue(const ServeBind& sb, const pkv_plan_t* plan, cudaStream_t s) {
     if (sb.pr.batch == 0) return PKV_OK;
     char* d = static_cast<char*>(sb.dev_in);
     void* out = sb.out_mapped ? sb.out_mapped : sb.dev_out;
+    pkv_plan_t run = *plan;
     if (sb.in_mapped) {
         if (launch_stage_copy(sb.in_mapped, sb.dev_in, sb.total, s) != cudaSuccess) return PKV_E_CUDA;
+        run.flags |= PKV_PLAN_INPUTS_AFTER_PREV;  // the decode's set-up overlaps the copy kernel
     } else if (cudaMemcpyAsync(sb.dev_in, sb.host_in, sb.total, cudaMemcpyHostToDevice, s) != cudaSuccess) {
         return PKV_E_CUDA;
     }
-    int rc = decode_step(plan, &sb.pr, d + sb.off[0], d + sb.off[1], d + sb.off[2], sb.k_pool, sb.v_pool,
+    int rc = decode_step(&run, &sb.pr, d + sb.off[0], d + sb.off[1], d + sb.off[2], sb.k_pool, sb.v_pool,
                          reinterpret_cast<const int32_t*>(d + sb.off[3]),
                          reinterpret_cast<const int32_t*>(d + sb.off[4]), sb.scale, sb.ws, sb.ws_bytes, out, s, false);
     if (rc != PKV_OK) return rc;

@@ -402,6 +402,7 @@ __global__ void __launch_bounds__((NCW + 3) * 32, ctas_per_sm(G)) decode_kernel(
     if (warp == NCW + 1 || warp == NCW + 2) {
         StaticTask k;
         int len = 0;
+        if (p.inputs_after_wait) grid_dependency_wait();  // the kernel before may still be writing the inputs
         pre_ok = first_task(p, lane, k, len);
         if (warp == NCW + 2 && lane == 0) {
             for (int i = 0; i < NTS; ++i) mbar_init(&tq[i], 1);

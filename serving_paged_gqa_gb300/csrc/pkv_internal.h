@@ -43,6 +43,7 @@ struct DecodeParams {
     int32_t fuse_merge;         // 1: the last task of each (row, KV head) merges its states and writes out
     int32_t list_in_decode;     // workqueue: derive the compact list from seq_lens in every CTA
     int32_t overlap_prev;       // launched to overlap the kernel before it: q is read only after griddepcontrol.wait
+    int32_t inputs_after_wait;  // launched to overlap the kernel before it: nothing is read before griddepcontrol.wait
     float scale_log2;           // scale * log2(e): scores are kept in base-2 units inside the kernel
 };
 

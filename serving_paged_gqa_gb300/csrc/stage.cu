@@ -6,12 +6,16 @@
 #include <algorithm>
 
 #include "pkv_internal.h"
+#include "pkv_ptx.cuh"
 
 namespace pkv {
 namespace {
 
 __global__ void __launch_bounds__(256) stage_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                                                          size_t n16) {
+    // the decode launched after this grid may start its set-up now; it reads the copied input only after waiting
+    // for this grid's completion
+    grid_launch_dependents();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
         dst[i] = src[i];
 }

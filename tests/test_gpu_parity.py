@@ -279,6 +279,10 @@ def test_api_rejects_bad_arguments_before_launch():
     with pytest.raises(pkv.PkvError) as e:
         pkv.pkv_decode_step(plan, step.problem, mis, step.k, step.v, step.bt, step.lens, step.scale, ws, out)
     assert e.value.code == -5
+    plan.flags = 0x4  # no such flag
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_decode_step(plan, step.problem, step.q, step.k, step.v, step.bt, step.lens, step.scale, ws, out)
+    assert e.value.code == -1
 
 
 # ------------------------------------------------------------------------------------------- fused vs separate merge
@@ -635,3 +639,36 @@ def test_serve_session_evicts_the_least_recently_used_graph():
     assert session.stats() == (n + 1, n + 2)
     assert pkv.pkv_read_status(ws) == 0
     session.close()
+
+
+@pytest.mark.parametrize("name,seed,t,variant,chunk,fused", [
+    ("b1_bucketed", 7, 3, None, 0, 0), ("b8_bimodal", 5, 4, None, 0, 0), ("b8_zipf", 8, 2, WQ, 12, 1),
+    ("tiny", 4, 0, SINGLE, 1, 0), ("b4_bimodal", 6, 1, SPLIT, 32, 1)])
+def test_inputs_written_by_the_kernel_before(name, seed, t, variant, chunk, fused):
+    """PKV_PLAN_INPUTS_AFTER_PREV: q, the block table and the lengths are written by a kernel enqueued just before
+    the step (their buffers poisoned first: NaN query rows, a block table of -1, zero lengths), and the step, which
+    may start while that kernel runs, must read them only after it: the output matches the oracle, no status."""
+    tr = make_trace(name, seed, steps=t + 1)
+    step = Step(tr, t)
+    plan = step.plan() if variant is None else step.plan(variant, chunk)
+    if plan.variant != SINGLE:
+        plan.fuse_merge = fused
+    plan.flags = pkv.PKV_PLAN_INPUTS_AFTER_PREV
+    ws = pkv.alloc_workspace(plan.ws_bytes)
+    q = torch.full_like(step.q, float("nan"))
+    bt = torch.full_like(step.bt, -1)
+    lens = torch.zeros_like(step.lens)
+    out = torch.full_like(step.q, float("nan"))
+    for i in range(2):
+        torch.cuda.synchronize()
+        torch.add(step.q, 0, out=q)  # kernels (not copies), the last one immediately before the step
+        torch.add(step.bt, 0, out=bt)
+        torch.add(step.lens, 0, out=lens)
+        pkv.pkv_decode_step(plan, step.problem, q, step.k, step.v, bt, lens, step.scale, ws, out)
+        torch.cuda.synchronize()
+        assert_close(out, step.reference(), f"{name} inputs after the kernel before, run {i}")
+        assert pkv.pkv_read_status(ws) == 0
+        q.fill_(float("nan"))
+        bt.fill_(-1)
+        lens.zero_()
+        out.fill_(float("nan"))
