@@ -302,10 +302,11 @@ def mean_regret(c: dict, groups) -> float:
     return float(np.mean([np.mean(v) for v in per.values()]))
 
 
-def refine(rows, c: dict, seed: int = 0, restarts: int = 6):
+def refine(rows, c: dict, seed: int = 0, restarts: int = 6, also: dict | None = None):
     """Refines least-squares constants towards the policy's purpose: ranking the candidates of a step. Nelder-Mead on
-    the logarithms of the constants minimises the calibration steps' mean regret (mean_regret), from the
-    least-squares point and a few seeded perturbations of the best point so far."""
+    the logarithms of the constants minimises the calibration steps' mean regret (mean_regret), from the better of
+    the least-squares point and `also` (the constants in force), then from a few seeded perturbations of the best
+    point so far."""
     from scipy.optimize import minimize
 
     groups = step_groups(rows)
@@ -322,14 +323,23 @@ def refine(rows, c: dict, seed: int = 0, restarts: int = 6):
         return mean_regret(consts(x), groups)
 
     x0 = np.clip(np.log(np.array([max(c[k], 1e-4) for k in keys])), lo, hi)
-    best_x, best_f = x0, obj(x0)
+    f0 = obj(x0)
+    best_x, best_f = x0, f0
+    if also is not None:
+        xa = np.clip(np.log(np.array([max(also[k], 1e-4) for k in keys])), lo, hi)
+        fa = obj(xa)
+        if fa < best_f:
+            best_x, best_f = xa, fa
     rng = np.random.default_rng(seed)
     for trial in range(restarts):
         xs = best_x + (rng.normal(0.0, 0.3, len(keys)) if trial else 0.0)
         res = minimize(obj, xs, method="Nelder-Mead", options={"maxiter": 1500, "xatol": 1e-3, "fatol": 1e-5})
         if res.fun < best_f:
             best_x, best_f = res.x, float(res.fun)
-    return consts(best_x), {"calibration_regret_lsq": obj(x0), "calibration_regret": best_f}
+    stats = {"calibration_regret_lsq": f0, "calibration_regret": best_f}
+    if also is not None:
+        stats["calibration_regret_in_force"] = fa
+    return consts(best_x), stats
 
 
 def write_constants(c: dict, stats: dict, source: str):
@@ -433,8 +443,9 @@ def main(argv=None):
         import serving_paged_gqa_gb300 as pkv
 
         rows = load_rows(args.sweep)
-        c, stats = fit(rows, policy_constants(pkv))
-        c, rstats = refine(rows, c)
+        in_force = policy_constants(pkv)
+        c, stats = fit(rows, in_force)
+        c, rstats = refine(rows, c, also=in_force)
         stats.update(rstats)
         seeds = sorted({r["seed"] for r in rows})
         write_constants(c, stats, f"least squares on {stats['rows']} timed candidate plans, then regret-refined on "

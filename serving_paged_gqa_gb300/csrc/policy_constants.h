@@ -1,7 +1,7 @@
 // Cost-model constants of pkv_policy_default. Written by serving_paged_gqa_gb300/calibrate.py (fit) from
 // the calibration sweep; rebuild the library after changing them.
 #pragma once
-#define PKV_FIT_SOURCE "least squares on 2791 timed candidate plans, then regret-refined on every candidate, seeds [0, 1, 2, 3, 4]"
+#define PKV_FIT_SOURCE "least squares on 2787 timed candidate plans, then regret-refined on every candidate, seeds [0, 1, 2, 3, 4]"
 #define PKV_FIT_LAUNCH_US 6.68741
 #define PKV_FIT_HBM_GBS 6800
 #define PKV_FIT_CTA_GBS 27.9217
