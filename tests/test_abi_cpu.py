@@ -253,3 +253,19 @@ def test_session_with_an_empty_batch_runs_without_the_device():
     assert lib.pkv_session_stats(h, ctypes.byref(n1), ctypes.byref(n2)) == 0
     assert (n1.value, n2.value) == (0, 0)
     assert lib.pkv_session_destroy(h) == 0
+
+
+def test_policy_refinement_never_ends_worse_than_the_constants_in_force():
+    """calibrate.refine on a slice of the committed calibration sweep: its result's mean regret is at most that of
+    the least-squares start and of the constants in force (`also`), whichever is lower."""
+    from serving_paged_gqa_gb300 import calibrate
+
+    rows = calibrate.load_rows(os.path.join(ROOT, "serving_paged_gqa_gb300", "policy", "calibration_sweep.json"))
+    rows = [r for r in rows if r["seed"] == 0]
+    in_force = calibrate.policy_constants(pkv)
+    lsq, _ = calibrate.fit(rows, in_force)
+    groups = calibrate.step_groups(rows)
+    got, stats = calibrate.refine(rows, lsq, restarts=1, also=in_force)
+    best_start = min(calibrate.mean_regret(lsq, groups), calibrate.mean_regret(in_force, groups))
+    assert calibrate.mean_regret(got, groups) <= best_start + 1e-12
+    assert abs(stats["calibration_regret_in_force"] - calibrate.mean_regret(in_force, groups)) < 1e-12
