@@ -672,3 +672,44 @@ def test_inputs_written_by_the_kernel_before(name, seed, t, variant, chunk, fuse
         bt.fill_(-1)
         lens.zero_()
         out.fill_(float("nan"))
+
+
+def test_serve_session_inside_a_callers_capture():
+    """A ServeSession step run while the caller captures the stream (torch.cuda.graph): the session enqueues the
+    launches into the caller's capture instead of its own graph (its counters do not move), and replaying the caller's
+    graph computes the step: out in host memory matches the oracle, the new token's K/V is appended."""
+    tr = make_trace("b8_bimodal", 5, steps=1)
+    base = Step(tr, 0, poison=False)
+    kp, vp = tr.host_pools()
+    B, Hq, d = tr.batch, tr.hq, tr.d
+    lens, bt = tr.seq_lens(0), tr.block_table(0)
+    ws = pkv.alloc_workspace(pkv.pkv_plan(base.problem, lens, base.sms).ws_bytes)
+    _, total = pkv.pkv_step_input_layout(base.problem)
+    dev_in = torch.empty(total, dtype=torch.uint8, device="cuda")
+    dev_out = torch.empty((B, Hq, d), dtype=torch.float16, device="cuda")
+    host_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    host_out = torch.empty((B, Hq, d), dtype=torch.float16).pin_memory()
+    session = pkv.ServeSession(base.problem, host_in, dev_in, base.k, base.v, base.scale, ws, dev_out, host_out)
+    # one ordinary step first (the session captures its own graph of this plan)
+    _session_loop(session, base, tr, kp, vp, host_in, host_out, [0], tr.seq_lens, tr.block_table)
+    assert session.stats() == (1, 1)
+    rows = np.arange(B)
+    phys, slot = bt[rows, (lens - 1) // tr.ps], (lens - 1) % tr.ps
+    pi, si = torch.from_numpy(phys.astype(np.int64)).cuda(), torch.from_numpy(slot.astype(np.int64)).cuda()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        session.run(s)
+    assert session.stats() == (1, 1)
+    base.k[pi, si] = float("nan")
+    base.v[pi, si] = float("nan")
+    host_out.fill_(float("nan"))
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    ref = oracle.attention(tr.q(0), kp, vp, bt, lens, base.scale)
+    assert_close(host_out.cuda(), ref, "session step replayed from the caller's graph")
+    assert torch.equal(base.k[pi, si].cpu(), torch.from_numpy(kp[phys, slot]))
+    assert pkv.pkv_read_status(ws) == 0
+    session.close()
