@@ -370,13 +370,23 @@ def merge_used(pkv, plans) -> dict:
     return used
 
 
+def _mean_us(ms, has_kernel) -> float | None:
+    """Mean of the event-timed kernel over the steps that launch it (None if none does: an event pair with no
+    kernel between them reads ~2 us of event overhead, not a kernel)."""
+    sel = np.asarray(ms)[np.asarray(has_kernel, dtype=bool)]
+    return 1e3 * float(sel.mean()) if sel.size else None
+
+
 def summarize(pkv, wl, r, peak):
     plans = r["plans"]
     K = len(plans)
     tok = K * wl.B
     return {"by_tokens": by_tokens(wl, r),"tokens_per_s": tok / (r["step_ms"].sum() * 1e-3), "step_us_mean": 1e3 * float(r["step_ms"].mean()),
             "decode_us_mean": 1e3 * float(r["dec_ms"].mean()),
-            "merge_us_mean": 1e3 * float(r["merge_ms"].mean()), "build_us_mean": 1e3 * float(r["build_ms"].mean()),
+            "merge_us_mean": _mean_us(r["merge_ms"], [p.variant != pkv.PKV_VARIANT_SINGLE and not p.fuse_merge
+                                                      for p in plans]),
+            "build_us_mean": _mean_us(r["build_ms"], [p.variant == pkv.PKV_VARIANT_WORKQUEUE and not p.list_in_decode
+                                                      for p in plans]),
             "decode_frac": float(r["kv_bytes"].sum() / (r["dec_ms"].sum() * 1e-3)) / 1e9 / peak,
             "copy_same_bytes_us_mean": 1e3 * float(r["copy_ms"].mean()),
             "copy_same_bytes_frac": float(r["kv_bytes"].sum() / (r["copy_ms"].sum() * 1e-3)) / 1e9 / peak,
