@@ -713,3 +713,31 @@ def test_serve_session_inside_a_callers_capture():
     assert torch.equal(base.k[pi, si].cpu(), torch.from_numpy(kp[phys, slot]))
     assert pkv.pkv_read_status(ws) == 0
     session.close()
+
+
+@pytest.mark.parametrize("B", [pkv.PKV_MAX_ROWS_IN_DECODE, pkv.PKV_MAX_ROWS_IN_DECODE + 1, pkv.PKV_MAX_BATCH])
+def test_batch_limits(B):
+    """The largest batch whose workqueue the decode derives itself (256 rows), the first one that runs the worklist
+    builder (257) and the largest batch the library takes (4096): seeded lengths of 0 to 200 tokens (empty rows,
+    partial and exact pages); the policy's plan (the single pass, for rows this short) and the workqueue with the
+    fused merge both match the oracle, the builder's list is bit-exact, no status."""
+    r = rng_for(B, 777)
+    lens = r.integers(0, 201, size=B)
+    lens[::17] = 0
+    lens[1::23] = 16
+    step = Step(_Lens(lens, seed=B).trace, 0)
+    ref = step.reference()
+    plan = step.plan()  # short rows: the single pass
+    out, ws, status = step.run(plan)
+    assert status == 0
+    assert_close(out, ref, f"B={B} policy plan {plan.describe()}")
+    wq = step.plan(WQ, 4)
+    assert wq.list_in_decode == (1 if B <= pkv.PKV_MAX_ROWS_IN_DECODE else 0)
+    wq.fuse_merge = 1
+    out, ws, status = step.run(wq)
+    assert status == 0
+    assert_close(out, ref, f"B={B} workqueue, fused merge")
+    if not wq.list_in_decode:
+        got, _, _, _ = read_worklist(wq, ws)
+        want = oracle.worklist(step.lens_host, 16, step.tr.hkv, 4)
+        assert got.shape == want.shape and np.array_equal(got, want)
