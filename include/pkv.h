@@ -46,7 +46,8 @@
 extern "C" {
 #endif
 
-#define PKV_VERSION 2
+/* 3: serving session (pkv_session_*) and PKV_PLAN_INPUTS_AFTER_PREV; the structs are unchanged from 2. */
+#define PKV_VERSION 3
 
 #define PKV_OK 0
 #define PKV_E_INVAL (-1)        /* bad shape, negative size, inconsistent plan/problem */

@@ -41,7 +41,7 @@ def test_exports_every_declared_symbol():
 
 
 def test_version_and_errors():
-    assert pkv.pkv_version() == 2
+    assert pkv.pkv_version() == 3
     assert "null" in pkv.pkv_strerror(-3)
     assert pkv.pkv_strerror(0) == "ok"
 
