@@ -269,3 +269,28 @@ def test_policy_refinement_never_ends_worse_than_the_constants_in_force():
     best_start = min(calibrate.mean_regret(lsq, groups), calibrate.mean_regret(in_force, groups))
     assert calibrate.mean_regret(got, groups) <= best_start + 1e-12
     assert abs(stats["calibration_regret_in_force"] - calibrate.mean_regret(in_force, groups)) < 1e-12
+
+
+def test_session_step_refuses_a_workspace_smaller_than_the_plan():
+    """A session bound to a workspace smaller than the step's plan: pkv_session_step plans from the lengths in
+    host_in, returns PKV_E_WS_TOO_SMALL and enqueues nothing (the device pointers are never used)."""
+    import numpy as np
+
+    lib = pkv.load()
+    pr = pkv.make_problem(1, 32, 8, 128, 16, 1024, 512)
+    offs, total = pkv.pkv_step_input_layout(pr)
+    raw = np.zeros(total + 64, dtype=np.uint8)
+    base = (-raw.ctypes.data) % 64
+    host_in = raw[base:base + total]
+    host_in[offs[4]:offs[4] + 4] = np.array([4096], dtype=np.int32).view(np.uint8)
+    vp = ctypes.c_void_p
+    a256 = vp(1 << 20)  # aligned stand-ins for the device buffers
+    h = vp()
+    assert lib.pkv_session_create(ctypes.byref(pr), None, 152, vp(host_in.ctypes.data), a256, a256, a256,
+                                  ctypes.c_float(0.1), a256, 256, a256, a256, ctypes.byref(h)) == 0
+    plan = pkv.Plan()
+    assert lib.pkv_session_step(h, None, ctypes.byref(plan)) == -4  # PKV_E_WS_TOO_SMALL
+    assert plan.ws_bytes > 256 and plan.num_tasks > 0
+    n1, n2 = ctypes.c_int64(-1), ctypes.c_int64(-1)
+    assert lib.pkv_session_stats(h, ctypes.byref(n1), ctypes.byref(n2)) == 0 and (n1.value, n2.value) == (0, 0)
+    assert lib.pkv_session_destroy(h) == 0
